@@ -1,0 +1,134 @@
+"""CPU oracle of the local MoE layer (route, dispatch, SwiGLU expert FFN, combine).
+
+TEST INFRASTRUCTURE ONLY: the tests, `__graft_entry__.smoke()` and the
+benchmark's CPU-baseline leg use it; the product library never does.
+
+The arithmetic lives in `oracle.c` (plain C, fp64, OpenMP over tokens), which
+cites the passages of "Hosting Qwen on Blackwell" it follows. This module only
+marshals numpy arrays through ctypes.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+NONFINITE = 5
+
+
+def build(force=False):
+    """Compile liboracle.so with gcc (OpenMP when available)."""
+    src = os.path.join(_HERE, "oracle.c")
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(src):
+        return _SO
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", src, "-o", _SO + ".tmp", "-lm"]
+    r = subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True, text=True)
+    if r.returncode != 0:
+        subprocess.run(base, check=True)
+    os.replace(_SO + ".tmp", _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_SO)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        lib.oracle_route.argtypes = [i64, i32, i32, vp, vp, vp]
+        lib.oracle_route.restype = i32
+        lib.oracle_dispatch.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp]
+        lib.oracle_dispatch.restype = i64
+        lib.oracle_expert_ffn_rows.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp]
+        lib.oracle_expert_ffn_rows.restype = None
+        lib.oracle_combine_tokens.argtypes = [i32, i32, vp, vp, vp, vp, i64, vp]
+        lib.oracle_combine_tokens.restype = None
+        lib.oracle_moe_layer_tokens.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp]
+        lib.oracle_moe_layer_tokens.restype = i32
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dt):
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+def num_threads():
+    return int(_load().oracle_num_threads())
+
+
+def route(logits, k):
+    """-> (status, topk_idx int32 [T,k], topk_w float64 [T,k])"""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    idx = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    st = _load().oracle_route(T, E, k, _p(lg), _p(idx), _p(w))
+    return int(st), idx, w
+
+
+def dispatch(topk_idx, e0, e1):
+    """-> dict(counts, offsets, row_pair [R], pair_row [T*k], R)"""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    n = e1 - e0
+    counts = np.zeros(n, np.int32)
+    offsets = np.zeros(n + 1, np.int32)
+    row_pair = np.full(T * k, -1, np.int32)
+    pair_row = np.full(T * k, -1, np.int32)
+    R = _load().oracle_dispatch(T, k, e0, e1, _p(idx), _p(counts), _p(offsets), _p(row_pair), _p(pair_row))
+    if R < 0:
+        raise ValueError("oracle_dispatch: bad arguments")
+    return dict(counts=counts, offsets=offsets, row_pair=row_pair[:R].copy(), pair_row=pair_row, R=int(R))
+
+
+def expert_ffn_rows(x_perm, offsets, w_gate, w_up, w_down, row_lo=0, row_hi=None):
+    """FFN of grouped rows [row_lo, row_hi) -> float64 [rows, H]."""
+    xp = _c(x_perm, np.uint16)
+    H = xp.shape[1]
+    n, I, _ = w_gate.shape
+    if row_hi is None:
+        row_hi = int(offsets[-1])
+    off = _c(offsets, np.int32)
+    wg, wu, wd = _c(w_gate, np.uint16), _c(w_up, np.uint16), _c(w_down, np.uint16)
+    y = np.zeros((row_hi - row_lo, H), np.float64)
+    _load().oracle_expert_ffn_rows(H, I, n, _p(xp), _p(off), _p(wg), _p(wu), _p(wd), row_lo, row_hi, _p(y))
+    return y
+
+
+def combine_tokens(y_perm, pair_row, topk_w, tokens=None):
+    """Weighted combine of grouped bf16 rows -> float64 [ntok, H]."""
+    yp = _c(y_perm, np.uint16)
+    H = yp.shape[1]
+    tw = _c(topk_w, np.float32)
+    T, k = tw.shape
+    toks = np.arange(T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
+    pr = _c(pair_row, np.int32)
+    out = np.zeros((toks.size, H), np.float64)
+    _load().oracle_combine_tokens(H, k, _p(yp), _p(pr), _p(tw), _p(toks), toks.size, _p(out))
+    return out
+
+
+def moe_layer_tokens(logits, x, w_gate, w_up, w_down, k, e0, e1, tokens=None):
+    """Token-major full layer for the listed tokens -> (status, float64 [ntok, H])."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    xx = _c(x, np.uint16)
+    H = xx.shape[1]
+    I = w_gate.shape[1]
+    toks = np.arange(T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
+    wg, wu, wd = _c(w_gate, np.uint16), _c(w_up, np.uint16), _c(w_down, np.uint16)
+    out = np.zeros((toks.size, H), np.float64)
+    st = _load().oracle_moe_layer_tokens(H, I, E, k, e0, e1, _p(lg), _p(xx), _p(wg), _p(wu), _p(wd),
+                                         _p(toks), toks.size, _p(out))
+    return int(st), out
