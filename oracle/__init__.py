@@ -45,6 +45,8 @@ def _load():
         lib.oracle_dispatch.restype = i64
         lib.oracle_expert_ffn_rows.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp]
         lib.oracle_expert_ffn_rows.restype = None
+        lib.oracle_expert_ffn_rowlist.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp]
+        lib.oracle_expert_ffn_rowlist.restype = None
         lib.oracle_combine_tokens.argtypes = [i32, i32, vp, vp, vp, vp, i64, vp]
         lib.oracle_combine_tokens.restype = None
         lib.oracle_moe_layer_tokens.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp]
@@ -106,9 +108,22 @@ def expert_ffn_rows(x_perm, offsets, w_gate, w_up, w_down, row_lo=0, row_hi=None
     return y
 
 
+def expert_ffn_rowlist(x_perm, offsets, w_gate, w_up, w_down, rows):
+    """FFN of the listed grouped rows -> float64 [len(rows), H]."""
+    xp = _c(x_perm, np.uint16)
+    H = xp.shape[1]
+    n, I, _ = w_gate.shape
+    off = _c(offsets, np.int32)
+    rr = _c(rows, np.int64)
+    wg, wu, wd = _c(w_gate, np.uint16), _c(w_up, np.uint16), _c(w_down, np.uint16)
+    y = np.zeros((rr.size, H), np.float64)
+    _load().oracle_expert_ffn_rowlist(H, I, n, _p(xp), _p(off), _p(wg), _p(wu), _p(wd), _p(rr), rr.size, _p(y))
+    return y
+
+
 def combine_tokens(y_perm, pair_row, topk_w, tokens=None):
-    """Weighted combine of grouped bf16 rows -> float64 [ntok, H]."""
-    yp = _c(y_perm, np.uint16)
+    """Weighted combine of grouped fp32 rows -> float64 [ntok, H]."""
+    yp = _c(y_perm, np.float32)
     H = yp.shape[1]
     tw = _c(topk_w, np.float32)
     T, k = tw.shape

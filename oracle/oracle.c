@@ -176,11 +176,21 @@ void oracle_expert_ffn_rows(int H, int I, int n, const uint16_t* x_perm, const i
     }
 }
 
+/* Same as oracle_expert_ffn_rows for an explicit list of grouped rows. */
+void oracle_expert_ffn_rowlist(int H, int I, int n, const uint16_t* x_perm, const int32_t* offsets,
+                               const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                               const int64_t* rows, int64_t nrows, double* y) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t q = 0; q < nrows; ++q)
+        oracle_expert_ffn_rows(H, I, n, x_perm, offsets, w_gate, w_up, w_down, rows[q], rows[q] + 1, y + q * H);
+}
+
 /*
  * Combine for the listed tokens: out[q, :] = sum_{j=0..k-1, pair_row[t*k+j] >= 0}
- * topk_w[t,j] * y_perm[pair_row[t*k+j], :], t = tokens[q], summed in slot order.
+ * topk_w[t,j] * y_perm[pair_row[t*k+j], :], t = tokens[q], summed in slot order
+ * (y_perm holds fp32 expert-output rows).
  */
-void oracle_combine_tokens(int H, int k, const uint16_t* y_perm, const int32_t* pair_row,
+void oracle_combine_tokens(int H, int k, const float* y_perm, const int32_t* pair_row,
                            const float* topk_w, const int64_t* tokens, int64_t ntok, double* out) {
 #pragma omp parallel for schedule(static)
     for (int64_t q = 0; q < ntok; ++q) {
@@ -191,7 +201,7 @@ void oracle_combine_tokens(int H, int k, const uint16_t* y_perm, const int32_t* 
             int32_t r = pair_row[t * k + j];
             if (r < 0) continue;
             double w = (double)topk_w[t * k + j];
-            for (int h = 0; h < H; ++h) o[h] += w * bf16_widen(y_perm[(int64_t)r * H + h]);
+            for (int h = 0; h < H; ++h) o[h] += w * (double)y_perm[(int64_t)r * H + h];
         }
     }
 }

@@ -134,10 +134,10 @@ def test_combine_is_slot_ordered_weighted_gather():
     lg = synth.normal_f32(8, synth.TID_AUX, (T, E))
     st, idx, w64 = oracle.route(lg, k)
     d = oracle.dispatch(idx, 2, 7)
-    yp = synth.normal_bf16(8, synth.TID_AUX + 1, (max(d["R"], 1), H))
+    yp = synth.normal_f32(8, synth.TID_AUX + 1, (max(d["R"], 1), H))
     w32 = w64.astype(np.float32)
     out = oracle.combine_tokens(yp, d["pair_row"], w32)
-    yf = bf(yp).astype(np.float64)
+    yf = yp.astype(np.float64)
     for t in range(T):
         ref = np.zeros(H)
         for j in range(k):
@@ -156,3 +156,14 @@ def test_layer_nonfinite_status():
     lg[1, 2] = np.nan
     st, _ = oracle.moe_layer_tokens(lg, x, wg, wu, wd, k, 0, E)
     assert st == oracle.NONFINITE
+
+
+def test_rowlist_equals_row_range():
+    T, H, I, E, k = 20, 32, 16, 3, 2
+    x, lg, wg, wu, wd = small_problem(T, H, I, E, k, seed=10)
+    st, idx, w = oracle.route(lg, k)
+    d = oracle.dispatch(idx, 0, 3)
+    xp = x[d["row_pair"] // k]
+    full = oracle.expert_ffn_rows(xp, d["offsets"], wg, wu, wd)
+    rows = np.array([0, 5, d["R"] - 1, 3], np.int64)
+    assert np.array_equal(oracle.expert_ffn_rowlist(xp, d["offsets"], wg, wu, wd, rows), full[rows])
