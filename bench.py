@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the local MoE layer of one expert-parallel rank on GB300.
+
+One step = one pass of the whole hot path over one batch of seeded synthetic
+input: route -> dispatch -> gate/up GEMM + SwiGLU -> down GEMM -> combine, each
+launched through the C ABI on one stream with CUDA events between the calls
+(the same kernels moe_layer launches).  Inputs are resident in HBM; L2 is
+flushed (256 MiB write) between timed steps, outside the timed region.
+
+Prints one JSON line.  `value` is routed tokens/s (T / step time, summed over
+replicas for N > 1: every rank runs its own replica, no collective on the data
+path).  `e2e` is the same metric through moe_layer with host buffers: pinned
+host->device copies of x and logits and the device->host copy of the output
+inside the timed region.  `--impl reference` times the CPU oracle instead.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer routed tokens/s + TFLOP/s (prefill), weight GB/s (decode), 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["expert_routing_dispatch_gb300/csrc/grouped_ffn.cu", "expert_routing_dispatch_gb300/csrc/common.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="prefill_ep_rank")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0), "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config):
+    """DRAM bytes per gate/up launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_gate_up.{config}.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    kv = {}
+    for ln in lines:
+        if ln.startswith("- ") and ":" in ln:
+            k, v = ln[2:].split(":", 1)
+            kv[k.strip()] = v.strip().strip("`")
+    try:
+        if kv.get("kernel_source_sha256_16") != kernel_hash():
+            return None
+        return float(kv["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for ln in (self.out or "").splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), max=float(f[2]), power=float(f[3]), hw=f[5], hwt=f[6], swt=f[7],
+                                 pcap=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 200] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "power_w_max": max(r["power"] for r in rows)}
+
+
+def cpu_baseline(cfg, inp, seconds):
+    """The oracle as it stands, on a bounded sample of the workload's tokens."""
+    import numpy as np
+
+    import oracle
+
+    T, k, e0, e1 = cfg["T"], cfg["k"], cfg["e0"], cfg["e1"]
+
+    def run(ntok, start):
+        toks = (np.arange(ntok, dtype=np.int64) + start) % T
+        t0 = time.perf_counter()
+        st, _ = oracle.moe_layer_tokens(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], k, e0,
+                                        e1, tokens=toks)
+        assert st == 0
+        return time.perf_counter() - t0
+
+    probe = min(T, 64)
+    dt = run(probe, 0)
+    n = int(min(T, max(probe, probe * seconds / max(dt, 1e-6))))
+    dt = run(n, probe)
+    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} of {T} tokens (route + SwiGLU FFN of their local slots + combine, token-major, fp64)",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    """The CPU oracle timed as the reference arm (rank 0 only)."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import synth
+
+    cfg = synth.config(args.config)
+    inp = synth.make_inputs(cfg)
+    T, k, e0, e1 = cfg["T"], cfg["k"], cfg["e0"], cfg["e1"]
+    per_step = min(T, 128)
+    times = []
+    for i in range(args.warmup + args.steps):
+        toks = (np.arange(per_step, dtype=np.int64) + i * per_step) % T
+        t0 = time.perf_counter()
+        st, _ = oracle.moe_layer_tokens(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], k, e0, e1,
+                                        tokens=toks)
+        assert st == 0
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = per_step / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": workload_config(cfg, None),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{per_step} tokens per step of the {cfg['name']} workload"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg, R):
+    T, H, I, E, k, e0, e1 = (cfg[n] for n in ("T", "H", "I", "E", "k", "e0", "e1"))
+    c = {"workload": f"{cfg['name']}: T={T} H={H} I={I} E={E} top-{k}, local experts [{e0},{e1})",
+         "T": T, "H": H, "I": I, "E": E, "k": k, "e0": e0, "e1": e1, "l2": "256 MiB L2 flush between timed steps"}
+    if R is not None:
+        c["R_routed_rows"] = R
+    return c
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import expert_routing_dispatch_gb300 as moe
+    import synth
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    moe.lib()
+
+    cfg = synth.config(args.config)
+    T, H, I, E, k, e0, e1 = synth.dims_of(cfg)
+    n = e1 - e0
+    P = T * k
+    inp = synth.make_inputs(cfg)
+    g = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+    x, lg, wg, wu, wd = (g(inp[nm]) for nm in ("x", "logits", "w_gate", "w_up", "w_down"))
+    dims = moe.Dims(T, H, I, E, k, e0, e1)
+    i32, f32 = torch.int32, torch.float32
+    topk_idx = torch.empty((T, k), dtype=i32, device=dev)
+    topk_w = torch.empty((T, k), dtype=f32, device=dev)
+    counts = torch.empty(n, dtype=i32, device=dev)
+    offsets = torch.empty(n + 1, dtype=i32, device=dev)
+    row_pair = torch.empty(P, dtype=i32, device=dev)
+    pair_row = torch.empty(P, dtype=i32, device=dev)
+    x_perm = torch.empty((P, H), dtype=torch.int16, device=dev)
+    h = torch.empty((P, I), dtype=torch.int16, device=dev)
+    y_perm = torch.empty((P, H), dtype=f32, device=dev)
+    out = torch.empty((T, H), dtype=f32, device=dev)
+    status = torch.zeros(1, dtype=i32, device=dev)
+    dws = moe.alloc_workspace(moe.moe_dispatch_workspace_size(dims), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    names = ["route", "dispatch", "gate_up", "down", "combine"]
+    launches_per_step = 1 + 4 + 1 + 1 + 1
+
+    def step(evs):
+        evs[0].record(stream)
+        moe.moe_route(dims, lg, topk_idx, topk_w, status, stream=sh)
+        evs[1].record(stream)
+        moe.moe_dispatch(dims, x, topk_idx, counts, offsets, row_pair, pair_row, x_perm, dws, stream=sh)
+        evs[2].record(stream)
+        moe.moe_expert_gate_up(dims, x_perm, offsets, wg, wu, h, status, stream=sh)
+        evs[3].record(stream)
+        moe.moe_expert_down(dims, h, offsets, wd, y_perm, status, stream=sh)
+        evs[4].record(stream)
+        moe.moe_combine(dims, y_perm, pair_row, topk_w, out, stream=sh)
+        evs[5].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(mk())
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    all_evs = []
+    wall0 = time.perf_counter()
+    with ClockSampler(local_rank) as clk:
+        for _ in range(args.steps):
+            flush.zero_()  # outside the event bracket
+            evs = mk()
+            step(evs)
+            all_evs.append(evs)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    per_kernel = {nm: [] for nm in names}
+    step_ms = []
+    for evs in all_evs:
+        step_ms.append(evs[0].elapsed_time(evs[5]))
+        for i, nm in enumerate(names):
+            per_kernel[nm].append(evs[i].elapsed_time(evs[i + 1]))
+    t_step = sum(step_ms) / len(step_ms)
+    kern_ms = {nm: sum(v) / len(v) for nm, v in per_kernel.items()}
+    R = int(offsets[-1].item())
+    if world > 1:
+        tt = torch.tensor([t_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step_max = float(tt.item())
+    else:
+        t_step_max = t_step
+
+    # ---- end to end through moe_layer with host buffers
+    x_h = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+    lg_h = torch.from_numpy(inp["logits"]).pin_memory()
+    out_h = torch.empty((T, H), dtype=f32).pin_memory()
+    x_d = torch.empty_like(x)
+    lg_d = torch.empty_like(lg)
+    lws = moe.alloc_workspace(moe.moe_workspace_size(dims), dev)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        moe.moe_layer(dims, x_d, lg_d, wg, wu, wd, out, lws, status=status, stream=sh)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    t_e2e = sum(e2e_ms) / len(e2e_ms)
+    assert int(status.item()) == 0
+    if world > 1:
+        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    flop_gate_up = 4.0 * H * I * R
+    flop_layer = 6.0 * H * I * R
+    achieved = flop_gate_up / (kern_ms["gate_up"] * 1e-3) / 1e12 if R else 0.0
+    weight_bytes = 3.0 * H * I * 2 * int(np.count_nonzero(np.diff(offsets.cpu().numpy())))
+    traffic = recorded_traffic(args.config)
+    line = {
+        "metric": METRIC,
+        "value": world * T / (t_step_max * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_step_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "config": workload_config(cfg, R),
+        "e2e": {"value": world * T / (t_e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(inp["x"].nbytes + inp["logits"].nbytes),
+                "d2h_bytes_per_step": int(T * H * 4),
+                "note": "moe_layer with pinned host x/logits in and fp32 output back; expert weights resident"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"kernel": "grouped_ffn gate/up (tcgen05, SiLU*up epilogue)", "bound": "tensor",
+                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
+                     "traffic": traffic, "algorithmic_flop_per_launch": flop_gate_up},
+        "clocks": clk.summary(),
+        "detail": {
+            "kernel_ms": {nm: round(v, 4) for nm, v in kern_ms.items()},
+            "layer_tflops": flop_layer / (t_step * 1e-3) / 1e12,
+            "gemm_tflops": flop_layer / ((kern_ms["gate_up"] + kern_ms["down"]) * 1e-3) / 1e12,
+            "routed_rows_per_s": R / (t_step * 1e-3),
+            "weight_gbs": weight_bytes / (t_step * 1e-3) / 1e9,
+            "wall_s_timed_loop_incl_flush": round(wall, 4),
+            "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+        },
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

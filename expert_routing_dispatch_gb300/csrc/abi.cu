@@ -1,0 +1,225 @@
+// abi.cu -- the extern "C" entry points declared in include/moe.h: host-side
+// argument checks, workspace carving, then kernel launches on the caller's
+// stream.  No allocation, no stream synchronisation.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace moe {
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const moe_dims* d) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 1 || d->E < 1 || d->E > 1024 || d->k < 1 || d->k > 32 || d->k > d->E) return MOE_ERR_INVALID_ARG;
+    if (d->e0 < 0 || d->e1 <= d->e0 || d->e1 > d->E) return MOE_ERR_INVALID_ARG;
+    if ((long long)d->T * d->k >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+    if (d->H < 64 || d->I < 64 || d->H > 16384 || d->I > 16384 || d->H % 64 || d->I % 64) return MOE_ERR_INVALID_ARG;
+    // weight rows of all local experts must be addressable by a TMA coordinate
+    if ((long long)(d->e1 - d->e0) * (d->H > d->I ? d->H : d->I) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int check_device() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+size_t pairs_of(const moe_dims* d) { return (size_t)d->T * (size_t)d->k; }
+
+// moe_layer workspace carving (all pieces 256-byte aligned)
+struct LayerWs {
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* row_pair;
+    int32_t* pair_row;
+    uint16_t* x_perm;
+    float* y_perm;
+    void* dispatch_ws;
+    void* ffn_ws;
+    size_t dispatch_bytes, ffn_bytes, total;
+};
+
+LayerWs carve(const moe_dims* d, void* base) {
+    LayerWs w{};
+    const size_t P = pairs_of(d), n = (size_t)(d->e1 - d->e0);
+    uint8_t* p = static_cast<uint8_t*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* r = p ? p + off : nullptr;
+        off += align_up(bytes);
+        return r;
+    };
+    w.topk_idx = reinterpret_cast<int32_t*>(take(P * 4));
+    w.topk_w = reinterpret_cast<float*>(take(P * 4));
+    w.counts = reinterpret_cast<int32_t*>(take(n * 4));
+    w.offsets = reinterpret_cast<int32_t*>(take((n + 1) * 4));
+    w.row_pair = reinterpret_cast<int32_t*>(take(P * 4));
+    w.pair_row = reinterpret_cast<int32_t*>(take(P * 4));
+    w.x_perm = reinterpret_cast<uint16_t*>(take(P * (size_t)d->H * 2));
+    w.y_perm = reinterpret_cast<float*>(take(P * (size_t)d->H * 4));
+    w.dispatch_bytes = align_up(dispatch_scratch_bytes((long long)P, (int)n));
+    w.dispatch_ws = take(w.dispatch_bytes);
+    w.ffn_bytes = align_up(ffn_scratch_bytes((long long)P, d->I));
+    w.ffn_ws = take(w.ffn_bytes);
+    w.total = off;
+    return w;
+}
+
+bool ws_ok(const void* ws, size_t have, size_t need) {
+    if (need == 0) return true;
+    return ws && (reinterpret_cast<uintptr_t>(ws) % kAlign) == 0 && have >= need;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported device or size";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_NONFINITE: return "non-finite router logit";
+        case MOE_ERR_TIMEOUT: return "internal wait timed out";
+        default: return "unknown status";
+    }
+}
+
+size_t moe_dispatch_workspace_size(const moe_dims* d) {
+    if (check_dims(d) != MOE_OK) return 0;
+    return align_up(dispatch_scratch_bytes((long long)pairs_of(d), d->e1 - d->e0));
+}
+
+size_t moe_expert_ffn_workspace_size(const moe_dims* d) {
+    if (check_dims(d) != MOE_OK) return 0;
+    return align_up(ffn_scratch_bytes((long long)pairs_of(d), d->I));
+}
+
+size_t moe_workspace_size(const moe_dims* d) {
+    if (check_dims(d) != MOE_OK) return 0;
+    return carve(d, nullptr).total;
+}
+
+int moe_route(const moe_dims* d, const float* logits, int32_t* topk_idx, float* topk_w, int32_t* status_dev,
+              void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w)) return MOE_ERR_INVALID_ARG;
+    if ((st = check_device())) return st;
+    return launched(launch_route(logits, d->T, d->E, d->k, topk_idx, topk_w, status_dev, (cudaStream_t)stream));
+}
+
+int moe_dispatch(const moe_dims* d, const uint16_t* x, const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                 int32_t* row_pair, int32_t* pair_row, uint16_t* x_perm, void* ws, size_t ws_bytes, void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(x) || !aligned16(topk_idx) || !aligned16(counts) || !aligned16(offsets) || !aligned16(row_pair) ||
+        !aligned16(pair_row) || !aligned16(x_perm))
+        return MOE_ERR_INVALID_ARG;
+    if (!ws_ok(ws, ws_bytes, moe_dispatch_workspace_size(d))) return MOE_ERR_WORKSPACE;
+    if ((st = check_device())) return st;
+    return launched(launch_dispatch(x, topk_idx, d->T, d->H, d->k, d->e0, d->e1, counts, offsets, row_pair, pair_row,
+                                    x_perm, ws, (cudaStream_t)stream));
+}
+
+int moe_expert_ffn(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
+                   const uint16_t* w_up, const uint16_t* w_down, float* y_perm, void* ws, size_t ws_bytes,
+                   int32_t* status_dev, void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(x_perm) || !aligned16(offsets) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(y_perm))
+        return MOE_ERR_INVALID_ARG;
+    if (!ws_ok(ws, ws_bytes, moe_expert_ffn_workspace_size(d))) return MOE_ERR_WORKSPACE;
+    if ((st = check_device())) return st;
+    return launched(launch_expert_ffn(x_perm, offsets, w_gate, w_up, w_down, y_perm, (long long)pairs_of(d), d->H,
+                                      d->I, d->e1 - d->e0, ws, status_dev, (cudaStream_t)stream));
+}
+
+int moe_expert_gate_up(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
+                       const uint16_t* w_up, uint16_t* h, int32_t* status_dev, void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(x_perm) || !aligned16(offsets) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(h))
+        return MOE_ERR_INVALID_ARG;
+    if ((st = check_device())) return st;
+    return launched(launch_gate_up(x_perm, offsets, w_gate, w_up, h, (long long)pairs_of(d), d->H, d->I,
+                                   d->e1 - d->e0, status_dev, (cudaStream_t)stream));
+}
+
+int moe_expert_down(const moe_dims* d, const uint16_t* h, const int32_t* offsets, const uint16_t* w_down,
+                    float* y_perm, int32_t* status_dev, void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(h) || !aligned16(offsets) || !aligned16(w_down) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+    if ((st = check_device())) return st;
+    return launched(launch_down(h, offsets, w_down, y_perm, (long long)pairs_of(d), d->H, d->I, d->e1 - d->e0,
+                                status_dev, (cudaStream_t)stream));
+}
+
+int moe_combine(const moe_dims* d, const float* y_perm, const int32_t* pair_row, const float* topk_w, float* out,
+                void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(y_perm) || !aligned16(pair_row) || !aligned16(topk_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((st = check_device())) return st;
+    return launched(launch_combine(y_perm, pair_row, topk_w, d->T, d->H, d->k, out, (cudaStream_t)stream));
+}
+
+int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits, const uint16_t* w_gate, const uint16_t* w_up,
+              const uint16_t* w_down, float* out, int32_t* topk_idx_opt, float* topk_w_opt, void* ws, size_t ws_bytes,
+              int32_t* status_dev, void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(x) || !aligned16(logits) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(out))
+        return MOE_ERR_INVALID_ARG;
+    if ((topk_idx_opt && !aligned16(topk_idx_opt)) || (topk_w_opt && !aligned16(topk_w_opt)))
+        return MOE_ERR_INVALID_ARG;
+    const LayerWs need = carve(d, nullptr);
+    if (!ws_ok(ws, ws_bytes, need.total)) return MOE_ERR_WORKSPACE;
+    if ((st = check_device())) return st;
+    LayerWs w = carve(d, ws);
+    int32_t* idx = topk_idx_opt ? topk_idx_opt : w.topk_idx;
+    float* wt = topk_w_opt ? topk_w_opt : w.topk_w;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (launch_route(logits, d->T, d->E, d->k, idx, wt, status_dev, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_dispatch(x, idx, d->T, d->H, d->k, d->e0, d->e1, w.counts, w.offsets, w.row_pair, w.pair_row,
+                             w.x_perm, w.dispatch_ws, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_expert_ffn(w.x_perm, w.offsets, w_gate, w_up, w_down, w.y_perm, (long long)pairs_of(d), d->H, d->I,
+                               d->e1 - d->e0, w.ffn_ws, status_dev, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_combine(w.y_perm, w.pair_row, wt, d->T, d->H, d->k, out, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+// dispatch.cu -- K2: select the pairs routed to the local experts and group them
+// into per-expert GEMM buffers.
+//
+// "Hosting Qwen on Blackwell", section "Expert Parallel": the inputs are the
+// same on every rank, so dispatch only picks the tokens routed to this rank's
+// experts, gathers the routing information and stages those tokens in the
+// buffers the grouped MoE GEMM reads.
+//
+// The order is fixed (a stable counting sort): rows of local expert e are
+// offsets[e] .. offsets[e+1]-1 and hold their pairs p = t*k + j in ascending p.
+// Four kernels, no host round trip:
+//   a) count   : per-CTA histogram of local experts over a chunk of 2048 pairs
+//   b) scan    : counts, exclusive offsets, and each chunk's base row per expert
+//   c) scatter : warp-ordered ranks (match_any + popc) -> row_pair, pair_row
+//   d) gather  : token-major copy of x rows into x_perm with 16-byte vectors,
+//                reading each token's row once however many local slots it has
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kPairsPerWarp = 256;
+constexpr int kChunk = kWarps * kPairsPerWarp;  // pairs per CTA
+constexpr int kMaxLocal = 1024;
+
+__global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __restrict__ topk_idx, long long P,
+                                                             int e0, int n, int32_t* __restrict__ chunk_hist) {
+    __shared__ int hist[kMaxLocal];
+    for (int e = threadIdx.x; e < n; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    long long base = (long long)blockIdx.x * kChunk;
+    for (int i = threadIdx.x; i < kChunk; i += blockDim.x) {
+        long long p = base + i;
+        if (p < P) {
+            int e = __ldg(topk_idx + p) - e0;
+            if (e >= 0 && e < n) atomicAdd(&hist[e], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < n; e += blockDim.x) chunk_hist[(size_t)blockIdx.x * n + e] = hist[e];
+}
+
+// one CTA: thread e owns local expert e
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int n,
+                                                             int32_t* __restrict__ counts,
+                                                             int32_t* __restrict__ offsets) {
+    __shared__ int warp_tot[32];
+    const int e = threadIdx.x;
+    int total = 0;
+    if (e < n)
+        for (int c = 0; c < nchunks; ++c) {
+            int v = chunk_hist[(size_t)c * n + e];
+            chunk_hist[(size_t)c * n + e] = total;  // exclusive within the expert
+            total += v;
+        }
+    // block exclusive scan of totals over e
+    const int lane = e & 31, warp = e >> 5;
+    int incl = total;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        warp_tot[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    int excl = incl - total + (warp > 0 ? warp_tot[warp - 1] : 0);
+    if (e < n) {
+        counts[e] = total;
+        offsets[e] = excl;
+        if (e == n - 1) offsets[n] = excl + total;
+        for (int c = 0; c < nchunks; ++c) chunk_hist[(size_t)c * n + e] += excl;
+    }
+}
+
+__global__ void __launch_bounds__(256) dispatch_scatter_kernel(const int32_t* __restrict__ topk_idx, long long P,
+                                                               int e0, int n,
+                                                               const int32_t* __restrict__ chunk_base,
+                                                               int32_t* __restrict__ row_pair,
+                                                               int32_t* __restrict__ pair_row) {
+    __shared__ int cur[kWarps][kMaxLocal];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kWarps * n; i += blockDim.x) cur[i / n][i % n] = 0;
+    __syncthreads();
+    const long long wbase = (long long)blockIdx.x * kChunk + (long long)warp * kPairsPerWarp;
+    const unsigned lt = (1u << lane) - 1u;
+    // pass 1: per-warp counts
+    for (int s = 0; s < kPairsPerWarp; s += 32) {
+        long long p = wbase + s + lane;
+        int e = (p < P) ? __ldg(topk_idx + p) - e0 : -1;
+        bool local = (e >= 0 && e < n);
+        unsigned peers = __match_any_sync(0xffffffffu, local ? e : -1);
+        if (local && (peers & lt) == 0) cur[warp][e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // per-warp starting rows: chunk base + counts of the earlier warps
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+        int run = chunk_base[(size_t)blockIdx.x * n + e];
+        for (int w = 0; w < kWarps; ++w) {
+            int c = cur[w][e];
+            cur[w][e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    // pass 2: ranks in pair order
+    for (int s = 0; s < kPairsPerWarp; s += 32) {
+        long long p = wbase + s + lane;
+        bool valid = p < P;
+        int e = valid ? __ldg(topk_idx + p) - e0 : -1;
+        bool local = valid && e >= 0 && e < n;
+        unsigned peers = __match_any_sync(0xffffffffu, local ? e : -1);
+        int b = local ? cur[warp][e] : 0;
+        __syncwarp();
+        if (local) {
+            int row = b + __popc(peers & lt);
+            if ((peers & lt) == 0) cur[warp][e] = b + __popc(peers);
+            row_pair[row] = (int32_t)p;
+            pair_row[p] = row;
+        } else if (valid) {
+            pair_row[p] = -1;
+        }
+        __syncwarp();
+    }
+}
+
+// one CTA per token: read x[t] once, write it to each of its local rows
+__global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __restrict__ x, int T, int H8, int k,
+                                                              const int32_t* __restrict__ pair_row,
+                                                              uint4* __restrict__ x_perm) {
+    __shared__ int rows[32];
+    __shared__ int nrows;
+    const int t = blockIdx.x;
+    if (threadIdx.x < 32) {
+        int r = (threadIdx.x < k) ? __ldg(pair_row + (size_t)t * k + threadIdx.x) : -1;
+        unsigned m = __ballot_sync(0xffffffffu, r >= 0);
+        if (r >= 0) rows[__popc(m & ((1u << threadIdx.x) - 1u))] = r;
+        if (threadIdx.x == 0) nrows = __popc(m);
+    }
+    __syncthreads();
+    const int nr = nrows;
+    if (nr == 0) return;
+    const uint4* src = x + (size_t)t * H8;
+    for (int v = threadIdx.x; v < H8; v += blockDim.x) {
+        uint4 val = __ldg(src + v);
+        for (int i = 0; i < nr; ++i) x_perm[(size_t)rows[i] * H8 + v] = val;
+    }
+}
+
+}  // namespace
+
+size_t dispatch_scratch_bytes(long long pairs, int n) {
+    long long nchunks = (pairs + kChunk - 1) / kChunk;
+    return (size_t)(nchunks * n * (long long)sizeof(int32_t));
+}
+
+cudaError_t launch_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int H, int k, int e0, int e1,
+                            int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
+                            uint16_t* x_perm, void* scratch, cudaStream_t s) {
+    const long long P = (long long)T * k;
+    const int n = e1 - e0;
+    const int nchunks = (int)((P + kChunk - 1) / kChunk);
+    int32_t* chunk_hist = static_cast<int32_t*>(scratch);
+    dispatch_count_kernel<<<nchunks, 256, 0, s>>>(topk_idx, P, e0, n, chunk_hist);
+    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_hist, nchunks, n, counts, offsets);
+    dispatch_scatter_kernel<<<nchunks, 256, 0, s>>>(topk_idx, P, e0, n, chunk_hist, row_pair, pair_row);
+    dispatch_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), T, H / 8, k, pair_row,
+                                             reinterpret_cast<uint4*>(x_perm));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

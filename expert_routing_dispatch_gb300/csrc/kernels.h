@@ -1,0 +1,40 @@
+// kernels.h -- internal launchers of the libmoe kernels (called by abi.cu after
+// the host-side argument checks).  Every launcher only enqueues work on `s`.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// route.cu
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
+                         int32_t* status, cudaStream_t s);
+
+// dispatch.cu
+size_t dispatch_scratch_bytes(long long pairs, int n);
+cudaError_t launch_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int H, int k, int e0, int e1,
+                            int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
+                            uint16_t* x_perm, void* scratch, cudaStream_t s);
+
+// combine.cu
+cudaError_t launch_combine(const float* y_perm, const int32_t* pair_row, const float* topk_w, int T, int H, int k,
+                           float* out, cudaStream_t s);
+
+// grouped_ffn.cu
+size_t ffn_scratch_bytes(long long rows, int I);
+cudaError_t launch_expert_ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
+                              const uint16_t* w_up, const uint16_t* w_down, float* y_perm, long long rows, int H,
+                              int I, int n, void* scratch, int32_t* status, cudaStream_t s);
+
+cudaError_t launch_gate_up(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
+                           const uint16_t* w_up, uint16_t* h, long long rows, int H, int I, int n, int32_t* status,
+                           cudaStream_t s);
+cudaError_t launch_down(const uint16_t* h, const int32_t* offsets, const uint16_t* w_down, float* y_perm,
+                        long long rows, int H, int I, int n, int32_t* status, cudaStream_t s);
+
+// device query shared by the launchers
+int sm_count();
+
+}  // namespace moe

@@ -1,0 +1,164 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) local mixture-of-experts layer of one
+ * expert-parallel rank: route -> dispatch -> grouped SwiGLU expert FFN -> combine.
+ *
+ * The operations follow "Hosting Qwen on Blackwell" (Perplexity, 2026):
+ *   - section "Expert Parallel": inputs are replicated on every rank; dispatch
+ *     only selects the tokens routed to this rank's experts, gathers the routing
+ *     information and stages the tokens in the buffers the MoE GEMM reads;
+ *     combine first accumulates locally, with weights, the contributions of the
+ *     tokens routed to this rank's experts (the cross-rank all-reduce that
+ *     follows is not part of this library);
+ *   - same section: for decode the whole layer is one fused kernel, for prefill
+ *     it is split into several kernels;
+ *   - section "MoE GEMM": the expert GEMM is a grouped GEMM over the experts;
+ *   - section "Prefillers": T*k/E tokens reach each expert on average.
+ * The router formula and the SwiGLU expert body are not on those pages; this
+ * library computes softmax-over-logits top-k with renormalised weights and
+ * FFN_e(x) = W_down[e] (silu(W_gate[e] x) * (W_up[e] x)).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc'd or PyTorch CUDA
+ *     tensors), row-major, contiguous, 16-byte aligned.  bf16 tensors are passed
+ *     as raw 16-bit patterns (uint16_t).
+ *   - The caller allocates and owns every buffer, including the workspace; the
+ *     library never allocates or frees device memory and never synchronises the
+ *     stream.  `stream` is a cudaStream_t (NULL = legacy default stream); all
+ *     work is enqueued asynchronously on it.
+ *   - Argument errors detected on the host return a status and launch nothing.
+ *     Launch failures return MOE_ERR_CUDA.  Data-dependent errors (non-finite
+ *     logit, an internal wait that timed out) are written to the device word
+ *     *status_dev when one is given (first error wins, 0 is never written: the
+ *     caller clears it); outputs are then undefined but every write stays in
+ *     bounds.  Nothing aborts, traps or throws across the ABI.
+ *   - Weight pointers cover the LOCAL experts only: index 0 is expert e0.
+ *   - The routed row count R lives on the device (offsets[n] = R); buffers
+ *     sized for T*k rows always suffice.
+ *   - Requires an sm_103 device (GB300); otherwise MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* shape, range or null-pointer error            */
+    MOE_ERR_UNSUPPORTED = 2, /* device is not sm_103, or a size limit is hit  */
+    MOE_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small    */
+    MOE_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed          */
+    MOE_ERR_NONFINITE = 5,   /* (device status) a router logit is NaN or Inf  */
+    MOE_ERR_TIMEOUT = 6      /* (device status) an internal wait ran out      */
+} moe_status;
+
+/*
+ * Problem shape.  T tokens, hidden size H, expert intermediate size I, E experts
+ * in total, top-k routing, local expert range [e0, e1) (n = e1 - e0 experts).
+ * Limits: T >= 1, T*k < 2^31, 1 <= k <= min(E, 32), 1 <= E <= 1024,
+ * 0 <= e0 < e1 <= E, H and I multiples of 64, 64 <= H, I <= 16384.
+ */
+typedef struct {
+    int32_t T, H, I, E, k, e0, e1;
+} moe_dims;
+
+/* Human-readable name of a moe_status value (static storage). */
+const char* moe_status_string(int status);
+
+/* Workspace bytes needed by moe_dispatch / moe_expert_ffn / moe_layer for
+ * these dims; 0 if the dims are invalid.  Workspace must be 256-byte aligned. */
+size_t moe_dispatch_workspace_size(const moe_dims* d);
+size_t moe_expert_ffn_workspace_size(const moe_dims* d);
+size_t moe_workspace_size(const moe_dims* d);
+
+/*
+ * Routing ("Expert Parallel" section: the routing information dispatch gathers).
+ * For each token t: the k largest logits[t, :] in descending order, ties broken
+ * to the lower expert id (-0.0 ties +0.0); slot j holds the j-th pick.
+ * topk_w[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k picks, in fp32
+ * (= the softmax over all E logits renormalised over the picks).
+ *   logits    fp32  [T, E]  in
+ *   topk_idx  int32 [T, k]  out, global expert ids in [0, E)
+ *   topk_w    fp32  [T, k]  out
+ *   status_dev int32[1] or NULL: set to MOE_ERR_NONFINITE if a logit is NaN/Inf
+ */
+int moe_route(const moe_dims* d, const float* logits, int32_t* topk_idx, float* topk_w,
+              int32_t* status_dev, void* stream);
+
+/*
+ * Dispatch ("Expert Parallel" section: select the tokens routed to the local
+ * experts and stage them in the grouped GEMM buffers).  A pair p = t*k + j is
+ * local when e0 <= topk_idx[p] < e1.
+ *   counts    int32 [n]        out, local pairs per local expert
+ *   offsets   int32 [n+1]      out, exclusive prefix sum, offsets[n] = R
+ *   row_pair  int32 [T*k]      out, rows [0, R): the pair each grouped row holds;
+ *                              one expert's rows hold its pairs in ascending p
+ *   pair_row  int32 [T*k]      out, row of pair p, or -1 if p is not local
+ *   x_perm    bf16  [T*k, H]   out, rows [0, R): x_perm[r] = x[row_pair[r] / k]
+ *   ws        >= moe_dispatch_workspace_size(d) bytes of scratch
+ * Deterministic: identical inputs give identical outputs, bit for bit.
+ */
+int moe_dispatch(const moe_dims* d, const uint16_t* x, const int32_t* topk_idx,
+                 int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
+                 uint16_t* x_perm, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Grouped SwiGLU expert FFN ("MoE GEMM" section), on the grouped rows made by
+ * moe_dispatch: for each local expert e and row r in [offsets[e], offsets[e+1]):
+ *   h[r]      = bf16( silu(x_perm[r] . W_gate[e]^T) * (x_perm[r] . W_up[e]^T) )
+ *   y_perm[r] = h[r] . W_down[e]^T                                  (fp32)
+ * bf16 operands, fp32 accumulation on the tcgen05 tensor cores, SiLU*up in fp32,
+ * h rounded to bf16 (it is the second GEMM's operand), y kept in fp32.
+ *   x_perm   bf16 [T*k, H]; offsets int32 [n+1] (device, read by the kernels)
+ *   w_gate, w_up  bf16 [n, I, H]; w_down bf16 [n, H, I]
+ *   y_perm   fp32 [T*k, H] out (rows >= R are left untouched)
+ *   ws       >= moe_expert_ffn_workspace_size(d) bytes (holds h)
+ *   status_dev as in moe_route (MOE_ERR_TIMEOUT if an internal wait ran out)
+ */
+int moe_expert_ffn(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets,
+                   const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                   float* y_perm, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * The two halves of moe_expert_ffn, for callers that keep h themselves (or
+ * time the GEMMs apart).  Same row grouping, operands and rounding.
+ *   moe_expert_gate_up: h[r] = bf16( silu(x_perm[r] . W_gate[e]^T) * (x_perm[r] . W_up[e]^T) )
+ *                       h bf16 [T*k, I] out (rows >= R untouched)
+ *   moe_expert_down:    y_perm[r] = h[r] . W_down[e]^T,  y_perm fp32 [T*k, H] out
+ */
+int moe_expert_gate_up(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets,
+                       const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,
+                       int32_t* status_dev, void* stream);
+int moe_expert_down(const moe_dims* d, const uint16_t* h, const int32_t* offsets,
+                    const uint16_t* w_down, float* y_perm, int32_t* status_dev, void* stream);
+
+/*
+ * Combine ("Expert Parallel" and "MoE Dispatch - Combine" sections: weighted
+ * local accumulation).  For each token t, in slot order j = 0..k-1 and in fp32:
+ *   out[t] = sum_{j : pair_row[t*k+j] >= 0} topk_w[t, j] * y_perm[pair_row[t*k+j]]
+ * Tokens with no local pair get exact zeros.  out is fp32 [T, H], overwritten: it
+ * is this rank's partial sum, ready for a cross-rank all-reduce.
+ */
+int moe_combine(const moe_dims* d, const float* y_perm, const int32_t* pair_row,
+                const float* topk_w, float* out, void* stream);
+
+/*
+ * The whole local layer: moe_route, moe_dispatch, moe_expert_ffn, moe_combine
+ * enqueued back to back on `stream` with all intermediates in `ws`
+ * (>= moe_workspace_size(d) bytes).  topk_idx_opt / topk_w_opt, when not NULL,
+ * receive the routing ([T, k] each); when NULL the workspace holds it.
+ */
+int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits,
+              const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+              float* out, int32_t* topk_idx_opt, float* topk_w_opt,
+              void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,72 @@
+"""Shared helpers of the GPU parity tests: move seeded host inputs to the device,
+call the C-ABI steps, and compare against the oracle.  The oracle only ever sees
+host arrays made by `synth` or by `oracle` itself."""
+import functools
+
+import numpy as np
+
+import oracle
+import synth
+
+WEIGHT_TOL = lambda k: (k + 8) * 2.0 ** -24  # |w_gpu - w_oracle|, fp32 expf/sum/div vs fp64
+OUT_TOL = 2e-2  # max |gpu - oracle| <= OUT_TOL * RMS(oracle)
+
+
+def dev(a, device="cuda"):
+    import torch
+
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(device)
+
+
+def host(t, dtype=None):
+    a = t.detach().cpu().numpy()
+    if dtype is not None:
+        a = a.view(dtype)
+    return a
+
+
+@functools.lru_cache(maxsize=8)
+def inputs(name, **over):
+    cfg = synth.config(name, **dict(over))
+    return cfg, synth.make_inputs(cfg)
+
+
+@functools.lru_cache(maxsize=8)
+def oracle_routing(name, **over):
+    cfg, inp = inputs(name, **over)
+    st, idx, w = oracle.route(inp["logits"], cfg["k"])
+    assert st == 0
+    d = oracle.dispatch(idx, cfg["e0"], cfg["e1"])
+    return idx, w, d
+
+
+def sample_tokens(T, n, seed=0):
+    """All tokens when T <= n, else the first, the last and n-2 seeded others."""
+    if T <= n:
+        return np.arange(T, dtype=np.int64)
+    rest = synth.uniform_int(seed, synth.TID_AUX + 7, n - 2, T)
+    return np.unique(np.concatenate([[0, T - 1], rest]).astype(np.int64))
+
+
+def sample_rows(offsets, n_per_expert=3, extra=64, seed=0):
+    """First and last row of every non-empty expert plus seeded extra rows."""
+    off = np.asarray(offsets)
+    R = int(off[-1])
+    rows = []
+    for e in range(off.size - 1):
+        if off[e + 1] > off[e]:
+            rows += [off[e], off[e + 1] - 1]
+            if n_per_expert > 2 and off[e + 1] - off[e] > 2:
+                rows.append((off[e] + off[e + 1]) // 2)
+    if R > 0:
+        rows += list(synth.uniform_int(seed, synth.TID_AUX + 8, extra, R))
+    return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+def rel_err(got, ref):
+    rms = float(np.sqrt(np.mean(np.asarray(ref, np.float64) ** 2)))
+    err = float(np.abs(np.asarray(got, np.float64) - ref).max()) if np.size(ref) else 0.0
+    return err, rms

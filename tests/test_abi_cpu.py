@@ -1,0 +1,88 @@
+"""The C-ABI library loads, exports every symbol include/moe.h declares, and
+rejects bad arguments on the host before touching a GPU (CPU only: none of these
+calls reaches the CUDA runtime)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import expert_routing_dispatch_gb300 as m
+
+    m.build()
+    return m
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree(moe):
+    assert header_symbols() == sorted(moe.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(moe):
+    L = ctypes.CDLL(moe.LIB_PATH)
+    for name in header_symbols():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(moe):
+    for code in range(7):
+        assert moe.moe_status_string(code) != "unknown status"
+    assert moe.moe_status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(moe):
+    d = moe.Dims(6000, 4096, 1536, 128, 8, 0, 32)
+    P = 6000 * 8
+    assert moe.moe_expert_ffn_workspace_size(d) >= P * 1536 * 2
+    assert moe.moe_dispatch_workspace_size(d) >= ((P + 2047) // 2048) * 32 * 4
+    total = moe.moe_workspace_size(d)
+    assert total >= 2 * P * 4096 * 2 + P * 1536 * 2 + 4 * P * 4
+    assert total % 256 == 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=0), dict(k=0), dict(k=33, E=64), dict(k=9, E=8), dict(e0=-1), dict(e1=0), dict(e0=5, e1=5),
+    dict(e1=200), dict(H=100), dict(I=96), dict(H=0), dict(E=2000), dict(T=600000000),
+])
+def test_invalid_dims_rejected_without_gpu(moe, bad):
+    base = dict(T=64, H=256, I=128, E=16, k=4, e0=0, e1=16)
+    base.update(bad)
+    d = moe.Dims.of(base)
+    assert moe.moe_workspace_size(d) == 0
+    fake = 1 << 20  # a 16-byte aligned address that is never dereferenced
+    st = moe.lib().moe_route(ctypes.byref(d), fake, fake, fake, None, None)
+    assert st == 1  # MOE_ERR_INVALID_ARG
+
+
+def test_misaligned_or_null_pointers_rejected(moe):
+    d = moe.Dims(64, 256, 128, 16, 4, 0, 16)
+    L = moe.lib()
+    ok = 1 << 20
+    assert L.moe_route(ctypes.byref(d), ok + 4, ok, ok, None, None) == 1
+    assert L.moe_route(ctypes.byref(d), None, ok, ok, None, None) == 1
+    assert L.moe_combine(ctypes.byref(d), ok, ok, ok + 8, ok, None) == 1
+    assert L.moe_layer(ctypes.byref(d), ok, ok, ok, ok, ok, ok + 2, None, None, ok, 1 << 40, None, None) == 1
+
+
+def test_missing_workspace_rejected(moe):
+    d = moe.Dims(64, 256, 128, 16, 4, 0, 16)
+    L = moe.lib()
+    ok = 1 << 20
+    need = moe.moe_workspace_size(d)
+    assert L.moe_layer(ctypes.byref(d), ok, ok, ok, ok, ok, ok, None, None, None, need, None, None) == 3
+    assert L.moe_layer(ctypes.byref(d), ok, ok, ok, ok, ok, ok, None, None, ok, need - 1, None, None) == 3
+    assert L.moe_layer(ctypes.byref(d), ok, ok, ok, ok, ok, ok, None, None, ok + 16, need, None, None) == 3
+    nd = moe.moe_dispatch_workspace_size(d)
+    assert L.moe_dispatch(ctypes.byref(d), ok, ok, ok, ok, ok, ok, ok, None, nd, None) == 3
+    nf = moe.moe_expert_ffn_workspace_size(d)
+    assert L.moe_expert_ffn(ctypes.byref(d), ok, ok, ok, ok, ok, ok, ok, nf - 256, None, None) == 3
