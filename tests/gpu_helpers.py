@@ -66,6 +66,27 @@ def sample_rows(offsets, n_per_expert=3, extra=64, seed=0):
     return np.unique(np.asarray(rows, dtype=np.int64))
 
 
+def bf16_h_bound(inp, k, e0, e1, tokens, idx, w):
+    """Elementwise bound of |gpu - oracle| implied by the GPU's arithmetic: h is
+    rounded to bf16 (unit roundoff u = 2^-8) before the down GEMM, everything
+    else is fp32 (relative errors ~2^-20 here, below 10% of the main term), so
+    |err[t]| <= 1.1 * u * sum_j w_tj * (|W_down[e_j]| @ |h_tj|)."""
+    bf = synth.bf16_to_f32
+    H = inp["x"].shape[1]
+    out = np.zeros((len(tokens), H))
+    for q, t in enumerate(tokens):
+        xt = bf(inp["x"][t]).astype(np.float64)
+        for j in range(k):
+            e = int(idx[t, j])
+            if not (e0 <= e < e1):
+                continue
+            g = bf(inp["w_gate"][e - e0]).astype(np.float64) @ xt
+            u = bf(inp["w_up"][e - e0]).astype(np.float64) @ xt
+            h = np.abs(g / (1.0 + np.exp(-g)) * u)
+            out[q] += float(w[t, j]) * (np.abs(bf(inp["w_down"][e - e0]).astype(np.float64)) @ h)
+    return 1.1 * 2.0 ** -8 * out
+
+
 def rel_err(got, ref):
     rms = float(np.sqrt(np.mean(np.asarray(ref, np.float64) ** 2)))
     err = float(np.abs(np.asarray(got, np.float64) - ref).max()) if np.size(ref) else 0.0

@@ -1,13 +1,17 @@
 """GPU edge cases against the oracle, through the C ABI: T=1, k=1, k=E, E not a
 multiple of 32, ragged H/I tails, empty local range (R=0), all-tied logits,
 non-finite logits (device status), one token per expert, the largest E and k,
-determinism, and range decomposition (four local ranges sum to the full range)."""
+determinism, and range decomposition (four local ranges sum to the full range).
+
+Routing is bit-exact.  Layer outputs on these off-workload shapes are held to the
+elementwise bound that rounding h to bf16 implies (see gpu_helpers.bf16_h_bound);
+the six workloads themselves are held to 2e-2 * RMS in test_gpu_parity."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_helpers import OUT_TOL, WEIGHT_TOL, dev, host, inputs, rel_err, sample_tokens
+from gpu_helpers import WEIGHT_TOL, bf16_h_bound, dev, host, inputs, rel_err, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -63,8 +67,14 @@ def check_layer(moe, dims, inp, tokens=None):
     toks = np.arange(T) if tokens is None else tokens
     st, ref = oracle.moe_layer_tokens(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], k, e0, e1,
                                       tokens=toks)
+    # these shapes lie outside the six workloads: the bar is the elementwise bound
+    # implied by rounding h to bf16 (k = 1 has no averaging over slots)
+    bound = bf16_h_bound(inp, k, e0, e1, toks, ridx, rw) + 1e-6 * np.abs(ref).max()
+    diff = np.abs(out[toks].astype(np.float64) - ref)
     err, rms = rel_err(out[toks], ref)
-    assert (rms == 0 and err == 0) or err <= OUT_TOL * rms, f"{err:.3e} vs RMS {rms:.3e}"
+    print(f"EDGE {tup(dims)} max|gpu-oracle|/RMS = {err / max(rms, 1e-300):.3e}, "
+          f"max err/bound = {(diff / bound).max():.3f}")
+    assert np.all(diff <= bound)
     return out
 
 
