@@ -11,7 +11,7 @@ import ctypes
 import os
 
 __all__ = [
-    "MoeError", "Dims", "lib", "build", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+    "MoeError", "Dims", "lib", "build", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine",
     "moe_layer", "moe_expert_gate_up", "moe_expert_down", "moe_workspace_size", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
     "moe_status_string", "alloc_workspace", "EXPORTED",
 ]
@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmoe.so")
 
 # every symbol include/moe.h declares
 EXPORTED = ("moe_status_string", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
-            "moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_expert_gate_up",
+            "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_expert_gate_up",
             "moe_expert_down", "moe_combine", "moe_layer")
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
@@ -73,12 +73,13 @@ def lib():
             f.restype = sz
         L.moe_route.argtypes = [pd, vp, vp, vp, vp, vp]
         L.moe_dispatch.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.moe_dispatch_noalloc.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_ffn.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         L.moe_expert_gate_up.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_down.argtypes = [pd, vp, vp, vp, vp, vp, vp]
         L.moe_combine.argtypes = [pd, vp, vp, vp, vp, vp]
         L.moe_layer.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
-        for f in (L.moe_route, L.moe_dispatch, L.moe_expert_ffn, L.moe_expert_gate_up, L.moe_expert_down,
+        for f in (L.moe_route, L.moe_dispatch, L.moe_dispatch_noalloc, L.moe_expert_ffn, L.moe_expert_gate_up, L.moe_expert_down,
                   L.moe_combine, L.moe_layer):
             f.restype = i32
         _lib = L
@@ -149,6 +150,17 @@ def moe_dispatch(dims, x, topk_idx, counts, offsets, row_pair, pair_row, x_perm,
     nb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check(lib().moe_dispatch(ctypes.byref(d), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets), _ptr(row_pair),
                               _ptr(pair_row), _ptr(x_perm), _ptr(ws), nb, _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_noalloc(dims, x, topk_idx, counts, offsets, row_pair, pair_row, x_perm, stream=None):
+    """moe_dispatch without a workspace, for callers that cannot allocate device
+    memory: the scratch is a fixed 1 MiB array inside libmoe shared by all calls
+    (calls that overlap on the GPU race).  Too-large problems raise
+    MOE_ERR_UNSUPPORTED."""
+    d = Dims.of(dims)
+    _check(lib().moe_dispatch_noalloc(ctypes.byref(d), _ptr(x), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
+                                      _ptr(row_pair), _ptr(pair_row), _ptr(x_perm), _stream(stream)),
+           "moe_dispatch_noalloc")
 
 
 def moe_expert_ffn(dims, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, ws_bytes=None, status=None, stream=None):

@@ -150,6 +150,19 @@ int moe_dispatch(const moe_dims* d, const uint16_t* x, const int32_t* topk_idx, 
                                     x_perm, ws, (cudaStream_t)stream));
 }
 
+int moe_dispatch_noalloc(const moe_dims* d, const uint16_t* x, const int32_t* topk_idx, int32_t* counts,
+                         int32_t* offsets, int32_t* row_pair, int32_t* pair_row, uint16_t* x_perm, void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(x) || !aligned16(topk_idx) || !aligned16(counts) || !aligned16(offsets) || !aligned16(row_pair) ||
+        !aligned16(pair_row) || !aligned16(x_perm))
+        return MOE_ERR_INVALID_ARG;
+    if (!dispatch_noalloc_fits((long long)pairs_of(d), d->e1 - d->e0)) return MOE_ERR_UNSUPPORTED;
+    if ((st = check_device())) return st;
+    return launched(launch_dispatch_noalloc(x, topk_idx, d->T, d->H, d->k, d->e0, d->e1, counts, offsets, row_pair,
+                                            pair_row, x_perm, (cudaStream_t)stream));
+}
+
 int moe_expert_ffn(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
                    const uint16_t* w_up, const uint16_t* w_down, float* y_perm, void* ws, size_t ws_bytes,
                    int32_t* status_dev, void* stream) {

@@ -14,6 +14,8 @@
 //   c) scatter : warp-ordered ranks (match_any + popc) -> row_pair, pair_row
 //   d) gather  : token-major copy of x rows into x_perm with 16-byte vectors,
 //                reading each token's row once however many local slots it has
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -174,6 +176,63 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, i
     const int n = e1 - e0;
     const int nchunks = (int)((P + kChunk - 1) / kChunk);
     int32_t* chunk_hist = static_cast<int32_t*>(scratch);
+    dispatch_count_kernel<<<nchunks, 256, 0, s>>>(topk_idx, P, e0, n, chunk_hist);
+    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_hist, nchunks, n, counts, offsets);
+    dispatch_scatter_kernel<<<nchunks, 256, 0, s>>>(topk_idx, P, e0, n, chunk_hist, row_pair, pair_row);
+    dispatch_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), T, H / 8, k, pair_row,
+                                             reinterpret_cast<uint4*>(x_perm));
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Variant for callers that cannot allocate device memory.  The per-chunk
+// histograms live in this fixed array, which belongs to the library's device
+// module: every GPU that loads the library keeps these bytes until the process
+// exits.  All calls share it, so calls that overlap on the GPU race on it.
+// Nothing in it needs clearing: the count kernel writes every entry that the
+// scan and scatter kernels later read.
+static __device__ __align__(256) int32_t g_noalloc_chunk_hist[kNoAllocScratchInts];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_noalloc_chunk_hist on the current device, looked up once
+// per device (host code cannot use the symbol's host-side shadow as a pointer).
+cudaError_t noalloc_scratch(int32_t** out) {
+    static std::mutex mu;
+    static int32_t* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_chunk_hist);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+bool dispatch_noalloc_fits(long long pairs, int n) {
+    long long nchunks = (pairs + kChunk - 1) / kChunk;
+    return nchunks * (long long)n <= (long long)kNoAllocScratchInts;
+}
+
+cudaError_t launch_dispatch_noalloc(const uint16_t* x, const int32_t* topk_idx, int T, int H, int k, int e0, int e1,
+                                    int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
+                                    uint16_t* x_perm, cudaStream_t s) {
+    int32_t* chunk_hist = nullptr;
+    cudaError_t e = noalloc_scratch(&chunk_hist);
+    if (e != cudaSuccess) return e;
+    const long long P = (long long)T * k;
+    const int n = e1 - e0;
+    const int nchunks = (int)((P + kChunk - 1) / kChunk);
     dispatch_count_kernel<<<nchunks, 256, 0, s>>>(topk_idx, P, e0, n, chunk_hist);
     dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_hist, nchunks, n, counts, offsets);
     dispatch_scatter_kernel<<<nchunks, 256, 0, s>>>(topk_idx, P, e0, n, chunk_hist, row_pair, pair_row);

@@ -18,6 +18,13 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, i
                             int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
                             uint16_t* x_perm, void* scratch, cudaStream_t s);
 
+// size of the fixed scratch array used by moe_dispatch_noalloc (int32 entries, 1 MiB)
+constexpr int kNoAllocScratchInts = 1 << 18;
+bool dispatch_noalloc_fits(long long pairs, int n);
+cudaError_t launch_dispatch_noalloc(const uint16_t* x, const int32_t* topk_idx, int T, int H, int k, int e0, int e1,
+                                    int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
+                                    uint16_t* x_perm, cudaStream_t s);
+
 // combine.cu
 cudaError_t launch_combine(const float* y_perm, const int32_t* pair_row, const float* topk_w, int T, int H, int k,
                            float* out, cudaStream_t s);

@@ -107,6 +107,28 @@ int moe_dispatch(const moe_dims* d, const uint16_t* x, const int32_t* topk_idx,
                  uint16_t* x_perm, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_dispatch for callers that cannot allocate device memory -- for example a
+ * plug-in inside a host runtime that owns every device buffer and hands it no
+ * allocator, or a latency-critical serving loop where cudaMalloc is forbidden
+ * because it can synchronise the whole device.  The paper has no counterpart:
+ * it is an interface convenience of this library.
+ *
+ * Same arguments, outputs and determinism as moe_dispatch, minus the workspace:
+ * its scratch (per-chunk expert histograms) is a fixed 1 MiB array compiled
+ * into the library, which every GPU that loads the library keeps until the
+ * process exits.  Limit: ceil(T*k / 2048) * (e1 - e0) <= 262144, e.g. T*k up to
+ * 4,194,304 pairs with 128 local experts; larger problems return
+ * MOE_ERR_UNSUPPORTED without launching.  It never calls cudaMalloc or cudaFree.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the one array: calls whose work overlaps on the GPU (for instance on two
+ * streams) race and give undefined results; calls ordered on one stream are fine.
+ */
+int moe_dispatch_noalloc(const moe_dims* d, const uint16_t* x, const int32_t* topk_idx,
+                         int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
+                         uint16_t* x_perm, void* stream);
+
+/*
  * Grouped SwiGLU expert FFN ("MoE GEMM" section), on the grouped rows made by
  * moe_dispatch: for each local expert e and row r in [offsets[e], offsets[e+1]):
  *   h[r]      = bf16( silu(x_perm[r] . W_gate[e]^T) * (x_perm[r] . W_up[e]^T) )
