@@ -2,10 +2,12 @@
 """Benchmark of the local MoE layer of one expert-parallel rank on GB300.
 
 One step = one pass of the whole hot path over one batch of seeded synthetic
-input: route -> dispatch -> gate/up GEMM + SwiGLU -> down GEMM -> combine, each
-launched through the C ABI on one stream with CUDA events between the calls
-(the same kernels moe_layer launches).  Inputs are resident in HBM; L2 is
-flushed (256 MiB write) between timed steps, outside the timed region.
+input: route -> dispatch -> gate/up GEMM + SwiGLU -> down GEMM -> combine.  For
+prefill-sized workloads each step is launched through the C ABI on one stream
+with CUDA events between the calls (the same kernels moe_layer launches); for
+decode-sized ones (T*k <= MOE_FUSED_MAX_PAIRS) it is moe_layer's single fused
+launch.  Inputs are resident in HBM; L2 is flushed (256 MiB write) between
+timed steps, outside the timed region.
 
 Prints one JSON line.  `value` is routed tokens/s (T / step time, summed over
 replicas for N > 1: every rank runs its own replica, no collective on the data
@@ -29,7 +31,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer routed tokens/s + TFLOP/s (prefill), weight GB/s (decode), 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["expert_routing_dispatch_gb300/csrc/grouped_ffn.cu", "expert_routing_dispatch_gb300/csrc/common.cuh"]
+KERNEL_SOURCES = ["expert_routing_dispatch_gb300/csrc/grouped_ffn.cu", "expert_routing_dispatch_gb300/csrc/grouped_gemm.cuh",
+                  "expert_routing_dispatch_gb300/csrc/common.cuh"]
 
 
 def parse():
@@ -257,23 +260,36 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    names = ["route", "dispatch", "gate_up", "down", "combine"]
-    launches_per_step = 1 + 4 + 1 + 1 + 1
+    lws = moe.alloc_workspace(moe.moe_workspace_size(dims), dev)
+    fused = P <= moe.FUSED_MAX_PAIRS
+    if fused:
+        # decode-sized: moe_layer is one persistent launch (route..combine fused)
+        names = ["layer_fused"]
+        launches_per_step = 1
 
-    def step(evs):
-        evs[0].record(stream)
-        moe.moe_route(dims, lg, topk_idx, topk_w, status, stream=sh)
-        evs[1].record(stream)
-        moe.moe_dispatch(dims, x, topk_idx, counts, offsets, row_pair, pair_row, x_perm, dws, stream=sh)
-        evs[2].record(stream)
-        moe.moe_expert_gate_up(dims, x_perm, offsets, wg, wu, h, status, stream=sh)
-        evs[3].record(stream)
-        moe.moe_expert_down(dims, h, offsets, wd, y_perm, status, stream=sh)
-        evs[4].record(stream)
-        moe.moe_combine(dims, y_perm, pair_row, topk_w, out, stream=sh)
-        evs[5].record(stream)
+        def step(evs):
+            evs[0].record(stream)
+            moe.moe_layer(dims, x, lg, wg, wu, wd, out, lws, topk_idx=topk_idx, topk_w=topk_w, status=status,
+                          stream=sh)
+            evs[1].record(stream)
+    else:
+        names = ["route", "dispatch", "gate_up", "down", "combine"]
+        launches_per_step = 1 + 4 + 1 + 1 + 1
 
-    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        def step(evs):
+            evs[0].record(stream)
+            moe.moe_route(dims, lg, topk_idx, topk_w, status, stream=sh)
+            evs[1].record(stream)
+            moe.moe_dispatch(dims, x, topk_idx, counts, offsets, row_pair, pair_row, x_perm, dws, stream=sh)
+            evs[2].record(stream)
+            moe.moe_expert_gate_up(dims, x_perm, offsets, wg, wu, h, status, stream=sh)
+            evs[3].record(stream)
+            moe.moe_expert_down(dims, h, offsets, wd, y_perm, status, stream=sh)
+            evs[4].record(stream)
+            moe.moe_combine(dims, y_perm, pair_row, topk_w, out, stream=sh)
+            evs[5].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
     for _ in range(args.warmup):
         flush.zero_()
         step(mk())
@@ -299,12 +315,16 @@ def run_ours(args):
     per_kernel = {nm: [] for nm in names}
     step_ms = []
     for evs in all_evs:
-        step_ms.append(evs[0].elapsed_time(evs[5]))
+        step_ms.append(evs[0].elapsed_time(evs[-1]))
         for i, nm in enumerate(names):
             per_kernel[nm].append(evs[i].elapsed_time(evs[i + 1]))
     t_step = sum(step_ms) / len(step_ms)
     kern_ms = {nm: sum(v) / len(v) for nm, v in per_kernel.items()}
-    R = int(offsets[-1].item())
+    # routed rows and active local experts, counted from this run's routing
+    ti = topk_idx.flatten()
+    loc = ti[(ti >= e0) & (ti < e1)]
+    R = int(loc.numel())
+    active = int(torch.unique(loc).numel())
     if world > 1:
         tt = torch.tensor([t_step], dtype=torch.float64, device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -318,7 +338,6 @@ def run_ours(args):
     out_h = torch.empty((T, H), dtype=f32).pin_memory()
     x_d = torch.empty_like(x)
     lg_d = torch.empty_like(lg)
-    lws = moe.alloc_workspace(moe.moe_workspace_size(dims), dev)
 
     def e2e_step():
         x_d.copy_(x_h, non_blocking=True)
@@ -353,9 +372,23 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     flop_gate_up = 4.0 * H * I * R
     flop_layer = 6.0 * H * I * R
-    achieved = flop_gate_up / (kern_ms["gate_up"] * 1e-3) / 1e12 if R else 0.0
-    weight_bytes = 3.0 * H * I * 2 * int(np.count_nonzero(np.diff(offsets.cpu().numpy())))
-    traffic = recorded_traffic(args.config)
+    weight_bytes = 3.0 * H * I * 2 * active
+    if fused:
+        # HBM roofline of the fused launch: active experts' weights streamed once,
+        # plus x, logits and the fp32 output (intermediates stay in L2)
+        alg_bytes = weight_bytes + T * H * 2 + T * E * 4 + T * H * 4
+        achieved = alg_bytes / (kern_ms["layer_fused"] * 1e-3) / 1e9
+        roofline = {"kernel": "moe_layer_fused_kernel (route..combine, one cooperative launch)", "bound": "hbm",
+                    "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
+                    "traffic": None, "algorithmic_bytes_per_launch": alg_bytes}
+    else:
+        achieved = flop_gate_up / (kern_ms["gate_up"] * 1e-3) / 1e12 if R else 0.0
+        roofline = {"kernel": "grouped_ffn gate/up (tcgen05, SiLU*up epilogue)", "bound": "tensor",
+                    "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
+                    "traffic": recorded_traffic(args.config), "algorithmic_flop_per_launch": flop_gate_up}
+    gemm_ms = kern_ms["layer_fused"] if fused else kern_ms["gate_up"] + kern_ms["down"]
     line = {
         "metric": METRIC,
         "value": world * T / (t_step_max * 1e-3),
@@ -375,15 +408,14 @@ def run_ours(args):
                 "d2h_bytes_per_step": int(T * H * 4),
                 "note": "moe_layer with pinned host x/logits in and fp32 output back; expert weights resident"},
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"kernel": "grouped_ffn gate/up (tcgen05, SiLU*up epilogue)", "bound": "tensor",
-                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
-                     "traffic": traffic, "algorithmic_flop_per_launch": flop_gate_up},
+        "roofline": roofline,
         "clocks": clk.summary(),
         "detail": {
             "kernel_ms": {nm: round(v, 4) for nm, v in kern_ms.items()},
             "layer_tflops": flop_layer / (t_step * 1e-3) / 1e12,
-            "gemm_tflops": flop_layer / ((kern_ms["gate_up"] + kern_ms["down"]) * 1e-3) / 1e12,
+            "gemm_tflops": flop_layer / (gemm_ms * 1e-3) / 1e12,
+            "path": "fused" if fused else "split",
+            "active_local_experts": active,
             "routed_rows_per_s": R / (t_step * 1e-3),
             "weight_gbs": weight_bytes / (t_step * 1e-3) / 1e9,
             "wall_s_timed_loop_incl_flush": round(wall, 4),

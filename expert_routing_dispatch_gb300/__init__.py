@@ -13,7 +13,7 @@ import os
 __all__ = [
     "MoeError", "Dims", "lib", "build", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine",
     "moe_layer", "moe_expert_gate_up", "moe_expert_down", "moe_workspace_size", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
-    "moe_status_string", "alloc_workspace", "EXPORTED",
+    "moe_status_string", "alloc_workspace", "EXPORTED", "moe_testing_layer_stalled_barrier", "FUSED_MAX_PAIRS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -22,7 +22,9 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmoe.so")
 # every symbol include/moe.h declares
 EXPORTED = ("moe_status_string", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
             "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_expert_gate_up",
-            "moe_expert_down", "moe_combine", "moe_layer")
+            "moe_expert_down", "moe_combine", "moe_layer", "moe_testing_layer_stalled_barrier")
+
+FUSED_MAX_PAIRS = 8192  # MOE_FUSED_MAX_PAIRS in include/moe.h
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_NONFINITE", 6: "MOE_ERR_TIMEOUT"}
@@ -79,8 +81,9 @@ def lib():
         L.moe_expert_down.argtypes = [pd, vp, vp, vp, vp, vp, vp]
         L.moe_combine.argtypes = [pd, vp, vp, vp, vp, vp]
         L.moe_layer.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+        L.moe_testing_layer_stalled_barrier.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         for f in (L.moe_route, L.moe_dispatch, L.moe_dispatch_noalloc, L.moe_expert_ffn, L.moe_expert_gate_up, L.moe_expert_down,
-                  L.moe_combine, L.moe_layer):
+                  L.moe_combine, L.moe_layer, L.moe_testing_layer_stalled_barrier):
             f.restype = i32
         _lib = L
     return _lib
@@ -194,3 +197,14 @@ def moe_layer(dims, x, logits, w_gate, w_up, w_down, out, ws, ws_bytes=None, top
     nb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check(lib().moe_layer(ctypes.byref(d), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(out),
                            _ptr(topk_idx), _ptr(topk_w), _ptr(ws), nb, _ptr(status), _stream(stream)), "moe_layer")
+
+
+def moe_testing_layer_stalled_barrier(dims, x, logits, w_gate, w_up, w_down, out, ws, ws_bytes=None, status=None,
+                                      stream=None):
+    """Fault-injection hook: the fused layer with a grid barrier that cannot
+    complete; the kernel must report MOE_ERR_TIMEOUT in `status` and return."""
+    d = Dims.of(dims)
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check(lib().moe_testing_layer_stalled_barrier(ctypes.byref(d), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up),
+                                                   _ptr(w_down), _ptr(out), _ptr(ws), nb, _ptr(status),
+                                                   _stream(stream)), "moe_testing_layer_stalled_barrier")

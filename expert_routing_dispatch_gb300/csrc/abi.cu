@@ -59,6 +59,7 @@ struct LayerWs {
     float* y_perm;
     void* dispatch_ws;
     void* ffn_ws;
+    unsigned* sync;
     size_t dispatch_bytes, ffn_bytes, total;
 };
 
@@ -84,6 +85,7 @@ LayerWs carve(const moe_dims* d, void* base) {
     w.dispatch_ws = take(w.dispatch_bytes);
     w.ffn_bytes = align_up(ffn_scratch_bytes((long long)P, d->I));
     w.ffn_ws = take(w.ffn_bytes);
+    w.sync = reinterpret_cast<unsigned*>(take(64));
     w.total = off;
     return w;
 }
@@ -207,9 +209,9 @@ int moe_combine(const moe_dims* d, const float* y_perm, const int32_t* pair_row,
     return launched(launch_combine(y_perm, pair_row, topk_w, d->T, d->H, d->k, out, (cudaStream_t)stream));
 }
 
-int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits, const uint16_t* w_gate, const uint16_t* w_up,
-              const uint16_t* w_down, float* out, int32_t* topk_idx_opt, float* topk_w_opt, void* ws, size_t ws_bytes,
-              int32_t* status_dev, void* stream) {
+static int layer_impl(const moe_dims* d, const uint16_t* x, const float* logits, const uint16_t* w_gate,
+                      const uint16_t* w_up, const uint16_t* w_down, float* out, int32_t* topk_idx_opt,
+                      float* topk_w_opt, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream, int stall) {
     int st = check_dims(d);
     if (st) return st;
     if (!aligned16(x) || !aligned16(logits) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
@@ -217,6 +219,8 @@ int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits, const u
         return MOE_ERR_INVALID_ARG;
     if ((topk_idx_opt && !aligned16(topk_idx_opt)) || (topk_w_opt && !aligned16(topk_w_opt)))
         return MOE_ERR_INVALID_ARG;
+    const bool fused = (long long)pairs_of(d) <= MOE_FUSED_MAX_PAIRS;
+    if (stall && !fused) return MOE_ERR_INVALID_ARG;
     const LayerWs need = carve(d, nullptr);
     if (!ws_ok(ws, ws_bytes, need.total)) return MOE_ERR_WORKSPACE;
     if ((st = check_device())) return st;
@@ -224,15 +228,33 @@ int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits, const u
     int32_t* idx = topk_idx_opt ? topk_idx_opt : w.topk_idx;
     float* wt = topk_w_opt ? topk_w_opt : w.topk_w;
     cudaStream_t s = (cudaStream_t)stream;
+    if (fused)
+        return launched(launch_layer_fused(x, logits, w_gate, w_up, w_down, out, idx, wt, w.counts, w.offsets,
+                                           w.row_pair, w.pair_row, w.x_perm, static_cast<uint16_t*>(w.ffn_ws),
+                                           w.y_perm, w.sync, d->T, d->H, d->I, d->E, d->k, d->e0, d->e1,
+                                           status_dev, stall, s));
     if (launch_route(logits, d->T, d->E, d->k, idx, wt, status_dev, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_dispatch(x, idx, d->T, d->H, d->k, d->e0, d->e1, w.counts, w.offsets, w.row_pair, w.pair_row,
-                             w.x_perm, w.dispatch_ws, s) != cudaSuccess)
+                        w.x_perm, w.dispatch_ws, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_expert_ffn(w.x_perm, w.offsets, w_gate, w_up, w_down, w.y_perm, (long long)pairs_of(d), d->H, d->I,
-                               d->e1 - d->e0, w.ffn_ws, status_dev, s) != cudaSuccess)
+                          d->e1 - d->e0, w.ffn_ws, status_dev, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_combine(w.y_perm, w.pair_row, wt, d->T, d->H, d->k, out, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
+}
+
+int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits, const uint16_t* w_gate, const uint16_t* w_up,
+              const uint16_t* w_down, float* out, int32_t* topk_idx_opt, float* topk_w_opt, void* ws, size_t ws_bytes,
+              int32_t* status_dev, void* stream) {
+    return layer_impl(d, x, logits, w_gate, w_up, w_down, out, topk_idx_opt, topk_w_opt, ws, ws_bytes, status_dev,
+                      stream, 0);
+}
+
+int moe_testing_layer_stalled_barrier(const moe_dims* d, const uint16_t* x, const float* logits,
+                                      const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                                      float* out, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream) {
+    return layer_impl(d, x, logits, w_gate, w_up, w_down, out, nullptr, nullptr, ws, ws_bytes, status_dev, stream, 1);
 }
 
 }  // extern "C"

@@ -1,0 +1,61 @@
+// combine.cuh -- weighted local accumulation of one token (device function),
+// used by the combine kernel and by the fused decode kernel.
+//
+// "Hosting Qwen on Blackwell", sections "MoE Dispatch - Combine" and "Expert
+// Parallel": combine accumulates, with the routing weights, the contributions of
+// the tokens routed to this rank's experts (before a cross-rank all-reduce).
+//   out[t] = sum_{j=0..k-1, pair_row[t*k+j] >= 0} topk_w[t,j] * y_perm[pair_row[t*k+j]]
+// in fp32 registers, slot order fixed (deterministic); tokens without a local
+// slot get zeros.  16-byte loads and stores of 4 fp32.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct CombineSmem {
+    int rows[32];
+    float wts[32];
+    int nrows;
+};
+
+// The whole CTA (nthreads threads) combines token t.  `cg` selects L2-coherent
+// loads for indices written earlier in the same launch by other CTAs.
+__device__ __forceinline__ void combine_token(const float4* __restrict__ y_perm, const int32_t* pair_row,
+                                              const float* topk_w, int t, int H4, int k, float4* __restrict__ out,
+                                              CombineSmem& sm, bool cg) {
+    if (threadIdx.x < 32) {
+        const int j = threadIdx.x;
+        int r = -1;
+        float w = 0.f;
+        if (j < k) {
+            r = cg ? __ldcg(pair_row + (size_t)t * k + j) : __ldg(pair_row + (size_t)t * k + j);
+            w = cg ? __ldcg(topk_w + (size_t)t * k + j) : __ldg(topk_w + (size_t)t * k + j);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
+        if (r >= 0) {
+            const int q = __popc(m & ((1u << j) - 1u));  // keeps slot order
+            sm.rows[q] = r;
+            sm.wts[q] = w;
+        }
+        if (j == 0) sm.nrows = __popc(m);
+    }
+    __syncthreads();
+    const int nr = sm.nrows;
+    float4* o = out + (size_t)t * H4;
+    for (int v = threadIdx.x; v < H4; v += blockDim.x) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < nr; ++q) {
+            const float4 y = cg ? __ldcg(y_perm + (size_t)sm.rows[q] * H4 + v) : __ldg(y_perm + (size_t)sm.rows[q] * H4 + v);
+            const float w = sm.wts[q];
+            a.x = fmaf(w, y.x, a.x);
+            a.y = fmaf(w, y.y, a.y);
+            a.z = fmaf(w, y.z, a.z);
+            a.w = fmaf(w, y.w, a.w);
+        }
+        o[v] = a;
+    }
+    __syncthreads();  // sm is reused by the next token
+}
+
+}  // namespace moe

@@ -1,0 +1,305 @@
+// grouped_gemm.cuh -- device core of the grouped expert GEMMs on the tcgen05
+// tensor cores, shared by the split kernels (grouped_ffn.cu) and the fused
+// decode kernel (decode_fused.cu).
+//
+// "Hosting Qwen on Blackwell", section "MoE GEMM": the expert FFN is a grouped
+// GEMM over the experts, dense at prefill (~375 rows per expert, "Prefillers")
+// and bound by streaming the weights from HBM at decode ("Decoders").
+//
+// Two phases over the grouped rows made by dispatch:
+//   gate/up : acc[128 x 256] = x_perm[rows] . [W_gate[e] rows n..n+127 ; W_up[e] rows n..n+127]^T
+//             epilogue h = bf16(silu(acc[:, 0:128]) * acc[:, 128:256])   (fp32 math)
+//   down    : acc[128 x 256] = h[rows] . W_down[e][n..n+255]^T  ->  y_perm = acc (fp32)
+// Tiles are (expert, m-tile of 128 rows, n-tile); the tile table is built on
+// the device from the row offsets.  Within an expert the m-tiles of one n-tile
+// are consecutive, so CTAs running side by side share a weight tile through L2.
+//
+// CTA = 6 warps: warp 0 issues TMA loads (128-byte swizzle) into a 4-stage
+// shared-memory ring; warp 1 owns 512 TMEM columns (two 256-column fp32
+// accumulators) and one of its threads issues tcgen05.mma (M=128, N=256,
+// K=16); warps 2..5 drain TMEM with tcgen05.ld and run the epilogue while the
+// next tile accumulates into the other buffer.  Every wait is bounded: on
+// timeout the status word gets MOE_ERR_TIMEOUT and all roles bail out.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+namespace gemm {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int MAX_LOCAL = 1024;
+constexpr long long WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
+
+struct Ctl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int tile_start[MAX_LOCAL + 1];  // exclusive prefix of tiles per expert
+    int row_off[MAX_LOCAL + 1];     // grouped-row offsets of the local experts
+};
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
+
+struct Args {
+    void* out;        // h bf16 (gate/up) or y_perm fp32 (down), row-major [rows, out_cols]
+    int32_t* status;  // device status word or NULL
+    int n;            // local experts
+    int kblocks;      // K / 64
+    int ntiles_n;     // n-tiles per expert
+    int out_cols;     // I (gate/up) or H (down)
+    int b_rows;       // weight rows per expert in the B tensor map (I or H)
+    int n_step;       // output columns per n-tile (128 or 256)
+};
+
+// Per-thread pipeline counters; they carry over from one GEMM phase to the next
+// inside one launch so the mbarrier phases stay in step.
+struct Pipe {
+    int g;   // k-blocks loaded (producer) / consumed (MMA)
+    int it;  // tiles accumulated (MMA) / drained (epilogue)
+    int issued[STAGES];
+};
+
+struct TileCoord {
+    int e, mt, nt, cnt;
+};
+
+// Shared memory: 1024-aligned stage ring followed by the control block.
+__device__ __forceinline__ uint32_t ring_base(uint8_t* raw) { return (smem_u32(raw) + 1023u) & ~1023u; }
+__device__ __forceinline__ Ctl& ctl_of(uint8_t* raw) {
+    const uint32_t b = ring_base(raw);
+    return *reinterpret_cast<Ctl*>(raw + (b - smem_u32(raw)) + (size_t)STAGES * STAGE_BYTES);
+}
+
+// thread 0: barriers; warp 1: TMEM.  Caller syncs afterwards.
+__device__ __forceinline__ void init(Ctl& c) {
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&c.full[s]), 1);
+            mbar_init(smem_u32(&c.empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&c.tfull[a]), 1);
+            mbar_init(smem_u32(&c.tempty[a]), 4);
+        }
+        mbar_init(smem_u32(&c.drain), 1);
+        c.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+}
+
+__device__ __forceinline__ void pipe_reset(Pipe& p) {
+    p.g = 0;
+    p.it = 0;
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) p.issued[s] = 0;
+}
+
+// warp 0: tile_start from row_off (must be in shared memory already).
+__device__ __forceinline__ void build_tile_table(Ctl& c, int n, int ntiles_n) {
+    if ((threadIdx.x >> 5) != 0) return;
+    const int lane = threadIdx.x & 31;
+    int carry = 0;
+    for (int b0 = 0; b0 < n; b0 += 32) {
+        const int e = b0 + lane;
+        int v = 0;
+        if (e < n) v = ((c.row_off[e + 1] - c.row_off[e] + BM - 1) / BM) * ntiles_n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (e < n) c.tile_start[e + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) c.tile_start[0] = 0;
+}
+
+__device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_hint, TileCoord& tc) {
+    if (tile >= c.tile_start[n]) return false;
+    int e = e_hint;
+    while (c.tile_start[e + 1] <= tile) ++e;  // tiles increase monotonically per CTA
+    e_hint = e;
+    const int cnt = c.row_off[e + 1] - c.row_off[e];
+    const int mtiles = (cnt + BM - 1) / BM;
+    const int local = tile - c.tile_start[e];
+    tc.e = e;
+    tc.nt = local / mtiles;
+    tc.mt = local - tc.nt * mtiles;
+    tc.cnt = cnt;
+    return true;
+}
+
+// One GEMM phase, every thread of the CTA calls it and plays its role.
+template <int MODE>
+__device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const CUtensorMap* tmA,
+                                          const CUtensorMap* tmB0, const CUtensorMap* tmB1, const Args& args) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = args.n;
+    volatile int* abort_flag = &c.abort_flag;
+    auto a_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES); };
+    auto b_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES + A_BYTES); };
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            const uint64_t pol_a = l2_policy_evict_last();
+            const uint64_t pol_b = l2_policy_evict_first();
+            int e_hint = 0;
+            TileCoord tc;
+            bool ok = !*abort_flag;
+            for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
+                const int a_row = c.row_off[tc.e] + tc.mt * BM;
+                const int b_row = tc.e * args.b_rows + tc.nt * args.n_step;
+                for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
+                    const int s = p.g % STAGES, r = p.g / STAGES;
+                    if (!mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag, args.status, WAIT_LIMIT)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&c.full[s]);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    p.issued[s] = r + 1;
+                    tma_load_2d(a_addr(s), tmA, kb * BK, a_row, fb, pol_a);
+                    if (MODE == MODE_GATEUP) {
+                        tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
+                        tma_load_2d(b_addr(s) + B_BYTES / 2, tmB1, kb * BK, b_row, fb, pol_b);
+                    } else {
+                        tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            int e_hint = 0;
+            TileCoord tc;
+            bool ok = !*abort_flag;
+            for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++p.it) {
+                const int acc = p.it & 1, use = p.it >> 1;
+                if (!mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag, args.status,
+                                       WAIT_LIMIT))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
+                    const int s = p.g % STAGES, r = p.g / STAGES;
+                    if (!mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status, WAIT_LIMIT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = sdesc_k_sw128(a_addr(s) + kk * 32);
+                        const uint64_t bd = sdesc_k_sw128(b_addr(s) + kk * 32);
+                        tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+                    }
+                    tc_commit(smem_u32(&c.empty[s]));
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&c.tfull[acc]));
+            }
+        }
+    } else {
+        // ================= epilogue (warps 2..5, TMEM lane quarter = warp % 4) =================
+        const int q = warp & 3;
+        int e_hint = 0;
+        TileCoord tc;
+        for (int tile = blockIdx.x; !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++p.it) {
+            const int acc = p.it & 1, use = p.it >> 1;
+            if (!mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status, WAIT_LIMIT)) break;
+            tc_fence_after();
+            const int row_in_e = tc.mt * BM + q * 32 + lane;
+            const bool valid = row_in_e < tc.cnt;
+            const long long grow = (long long)c.row_off[tc.e] + row_in_e;
+            const uint32_t taddr = c.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const int col0 = tc.nt * args.n_step;
+            if (MODE == MODE_GATEUP) {
+                uint16_t* orow = static_cast<uint16_t*>(args.out) + grow * args.out_cols;
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 2; cc += 16) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(taddr + cc, g);
+                    tmem_ld16(taddr + BN / 2 + cc, u);
+                    tmem_ld_wait();
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                        const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                        const float h0 = g0 / (1.f + __expf(-g0)) * u0;
+                        const float h1 = g1 / (1.f + __expf(-g1)) * u1;
+                        pk[i] = pack_bf16x2(h0, h1);
+                    }
+                    if (valid && col0 + cc < args.out_cols) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + col0 + cc);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                }
+            } else {
+                float* orow = static_cast<float*>(args.out) + grow * args.out_cols;
+#pragma unroll 1
+                for (int cc = 0; cc < BN; cc += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + cc, v);
+                    tmem_ld_wait();
+                    if (valid && col0 + cc < args.out_cols) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + col0 + cc);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&c.tempty[acc]));
+        }
+        // the stores above are read later through TMA (async proxy) by other CTAs
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+}
+
+// After a __syncthreads: drain in-flight copies and MMAs (bounded), free TMEM.
+__device__ __forceinline__ void teardown(Ctl& c, Pipe& p, int32_t* status) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s)
+            if (p.issued[s] > 0) {
+                volatile int never = 0;
+                mbar_wait_bounded(smem_u32(&c.full[s]), (p.issued[s] - 1) & 1, &never, status, WAIT_LIMIT);
+            }
+    }
+    if (warp == 1) {
+        if (lane == 0) {
+            tc_commit(smem_u32(&c.drain));
+            volatile int never = 0;
+            mbar_wait_bounded(smem_u32(&c.drain), 0, &never, status, WAIT_LIMIT);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(c.tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace gemm
+}  // namespace moe

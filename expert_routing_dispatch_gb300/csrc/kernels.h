@@ -2,6 +2,7 @@
 // the host-side argument checks).  Every launcher only enqueues work on `s`.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -40,6 +41,18 @@ cudaError_t launch_gate_up(const uint16_t* x_perm, const int32_t* offsets, const
                            cudaStream_t s);
 cudaError_t launch_down(const uint16_t* h, const int32_t* offsets, const uint16_t* w_down, float* y_perm,
                         long long rows, int H, int I, int n, int32_t* status, cudaStream_t s);
+
+// TMA descriptor of a bf16 row-major [rows, cols] matrix: boxes of 64 columns
+// (128 B, 128-byte swizzle) x box_rows rows
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, int cols, int box_rows);
+
+// decode_fused.cu: the whole layer in one persistent cooperative launch
+cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uint16_t* w_gate, const uint16_t* w_up,
+                               const uint16_t* w_down, float* out, int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
+                               uint16_t* x_perm, uint16_t* h, float* y_perm, unsigned* sync, int T, int H, int I,
+                               int E, int k, int e0, int e1, int32_t* status, int stall_first_barrier,
+                               cudaStream_t s);
 
 // device query shared by the launchers
 int sm_count();

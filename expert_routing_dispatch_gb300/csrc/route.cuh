@@ -1,0 +1,99 @@
+// route.cuh -- per-token top-k routing (device function), used by the router
+// kernel and by the fused decode kernel.
+//
+// "Hosting Qwen on Blackwell", section "Expert Parallel": routing is the light
+// part of the EP kernel.  Per token: the k largest fp32 logits in descending
+// order, ties to the lower expert id; weights = softmax over the k picks (equal
+// to the full softmax renormalised over them).
+//
+// Selection is exact: each (logit, id) maps to a 64-bit key whose unsigned order
+// is "larger logit first, then lower id" (-0.0 folded onto +0.0), so each of the
+// k passes is a plain warp max over keys.  Lane l holds the logits of experts
+// l, l+32, l+64, ... in registers (coalesced loads).
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ uint32_t route_ordered_bits(float v) {
+    uint32_t u = __float_as_uint(v);
+    if ((u << 1) == 0) u = 0;  // -0.0 ties +0.0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t route_warp_max(uint64_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// The whole warp routes token t.  NPL = logits per lane, E <= 32 * NPL.
+template <int NPL>
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
+                                            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                            int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const float* row = logits + (size_t)t * E;
+    uint64_t key[NPL];
+    bool finite = true;
+#pragma unroll
+    for (int c = 0; c < NPL; ++c) {
+        const int e = c * 32 + lane;
+        if (e < E) {
+            const float v = __ldg(row + e);
+            finite &= isfinite(v);
+            key[c] = ((uint64_t)route_ordered_bits(v) << 32) | (uint32_t)(0xffffffffu - (uint32_t)e);
+        } else {
+            key[c] = 0;  // below every real key
+        }
+    }
+    if (__any_sync(0xffffffffu, !finite) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+
+    // k passes of warp argmax; lane j keeps the j-th pick
+    uint64_t mine = 0;
+    for (int j = 0; j < k; ++j) {
+        uint64_t best = 0;
+#pragma unroll
+        for (int c = 0; c < NPL; ++c) best = key[c] > best ? key[c] : best;
+        best = route_warp_max(best);
+#pragma unroll
+        for (int c = 0; c < NPL; ++c)
+            if (key[c] == best) key[c] = 0;  // remove the pick (keys are unique)
+        if (lane == j) mine = best;
+    }
+    const uint64_t top = __shfl_sync(0xffffffffu, mine, 0);
+    const int id = (int)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
+    const float v = (lane < k) ? __ldg(row + id) : 0.f;
+    const float m = __ldg(row + (int)(0xffffffffu - (uint32_t)(top & 0xffffffffu)));
+    const float ex = (lane < k) ? expf(v - m) : 0.f;
+    // sum over the k picks in slot order, the same sequential order in every lane
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+        topk_idx[(size_t)t * k + lane] = id;
+        topk_w[(size_t)t * k + lane] = ex / sum;
+    }
+}
+
+// Runtime choice of the register layout for E experts (E <= 1024).
+__device__ __forceinline__ void route_token_any(const float* logits, int t, int E, int k, int32_t* topk_idx,
+                                                float* topk_w, int32_t* status) {
+    if (E <= 32)
+        route_token<1>(logits, t, E, k, topk_idx, topk_w, status);
+    else if (E <= 64)
+        route_token<2>(logits, t, E, k, topk_idx, topk_w, status);
+    else if (E <= 128)
+        route_token<4>(logits, t, E, k, topk_idx, topk_w, status);
+    else if (E <= 256)
+        route_token<8>(logits, t, E, k, topk_idx, topk_w, status);
+    else if (E <= 512)
+        route_token<16>(logits, t, E, k, topk_idx, topk_w, status);
+    else
+        route_token<32>(logits, t, E, k, topk_idx, topk_w, status);
+}
+
+}  // namespace moe

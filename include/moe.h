@@ -168,16 +168,40 @@ int moe_expert_down(const moe_dims* d, const uint16_t* h, const int32_t* offsets
 int moe_combine(const moe_dims* d, const float* y_perm, const int32_t* pair_row,
                 const float* topk_w, float* out, void* stream);
 
+/* T*k at or below which moe_layer runs the fused single-launch (decode) path. */
+#define MOE_FUSED_MAX_PAIRS 8192
+
 /*
- * The whole local layer: moe_route, moe_dispatch, moe_expert_ffn, moe_combine
- * enqueued back to back on `stream` with all intermediates in `ws`
- * (>= moe_workspace_size(d) bytes).  topk_idx_opt / topk_w_opt, when not NULL,
- * receive the routing ([T, k] each); when NULL the workspace holds it.
+ * The whole local layer, all intermediates in `ws` (>= moe_workspace_size(d)
+ * bytes).  "Expert Parallel" section: for decode the whole kernel is fused into
+ * one, prefill is split into several kernels.  Accordingly:
+ *   - T*k <= MOE_FUSED_MAX_PAIRS: one persistent cooperative launch (one CTA per
+ *     SM) that routes, dispatches, runs both grouped GEMMs and combines, with
+ *     grid-wide barriers between the phases (plus a 8-byte memset of its barrier
+ *     words on the stream);
+ *   - otherwise moe_route, moe_dispatch, moe_expert_ffn and moe_combine back to back.
+ * Both give bit-identical results for the same inputs.  topk_idx_opt /
+ * topk_w_opt, when not NULL, receive the routing ([T, k] each); when NULL the
+ * workspace holds it.  status_dev: MOE_ERR_NONFINITE, or MOE_ERR_TIMEOUT if an
+ * internal wait (a grid barrier of the fused path) ran out.
  */
 int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits,
               const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
               float* out, int32_t* topk_idx_opt, float* topk_w_opt,
               void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * Testing hook for failure detection without a GPU fault: the fused path of
+ * moe_layer with its first grid-wide barrier told to wait for one CTA more than
+ * the grid holds, so that wait runs out (~1 s of GPU clock cycles).  The kernel
+ * then writes MOE_ERR_TIMEOUT to *status_dev, skips the remaining phases, frees
+ * its tensor memory and returns; the CUDA context stays usable.  Outputs are
+ * undefined.  Requires T*k <= MOE_FUSED_MAX_PAIRS (else MOE_ERR_INVALID_ARG).
+ */
+int moe_testing_layer_stalled_barrier(const moe_dims* d, const uint16_t* x, const float* logits,
+                                      const uint16_t* w_gate, const uint16_t* w_up,
+                                      const uint16_t* w_down, float* out, void* ws, size_t ws_bytes,
+                                      int32_t* status_dev, void* stream);
 
 #ifdef __cplusplus
 }
