@@ -52,6 +52,24 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
 
 
+def reduce_max(value, world, device=None):
+    """Max of a per-rank time over all ranks (only the bench's bookkeeping uses a
+    collective; the MoE data path has none)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, t_max_ms):
+    """Whole-job tokens/s: every rank processes its own replica of the workload."""
+    return world * tokens_per_rank / (t_max_ms * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -325,12 +343,7 @@ def run_ours(args):
     loc = ti[(ti >= e0) & (ti < e1)]
     R = int(loc.numel())
     active = int(torch.unique(loc).numel())
-    if world > 1:
-        tt = torch.tensor([t_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step_max = float(tt.item())
-    else:
-        t_step_max = t_step
+    t_step_max = reduce_max(t_step, world, dev)
 
     # ---- end to end through moe_layer with host buffers
     x_h = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
@@ -359,10 +372,7 @@ def run_ours(args):
         e2e_ms.append(a.elapsed_time(b))
     t_e2e = sum(e2e_ms) / len(e2e_ms)
     assert int(status.item()) == 0
-    if world > 1:
-        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = reduce_max(t_e2e, world, dev)
 
     if rank != 0:
         if world > 1:
@@ -391,7 +401,7 @@ def run_ours(args):
     gemm_ms = kern_ms["layer_fused"] if fused else kern_ms["gate_up"] + kern_ms["down"]
     line = {
         "metric": METRIC,
-        "value": world * T / (t_step_max * 1e-3),
+        "value": job_throughput(world, T, t_step_max),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -403,7 +413,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; random-init weights)",
         "config": workload_config(cfg, R),
-        "e2e": {"value": world * T / (t_e2e * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(world, T, t_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(inp["x"].nbytes + inp["logits"].nbytes),
                 "d2h_bytes_per_step": int(T * H * 4),
                 "note": "moe_layer with pinned host x/logits in and fp32 output back; expert weights resident"},

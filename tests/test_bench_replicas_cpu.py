@@ -1,0 +1,63 @@
+"""The multi-process (N > 1) bookkeeping of bench.py on CPU with gloo,
+world_size 2: the timing max over ranks, the whole-job throughput of N
+independent replicas, and the reference arm under torchrun (rank 0 alone
+prints one line, the other rank exits 0 without work)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local_ms = [2.0, 3.5][rank]  # the slower rank sets the job's time
+    t = bench.reduce_max(local_ms, world)
+    q.put((rank, t, bench.job_throughput(world, 6000, t)))
+    dist.destroy_process_group()
+
+
+def test_reduce_max_and_job_throughput_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [3.5, 3.5]
+    assert res[0][2] == pytest.approx(2 * 6000 / 3.5e-3)
+
+
+def test_single_rank_needs_no_collective():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.reduce_max(1.25, 1) == 1.25
+    assert bench.job_throughput(1, 256, 0.5) == pytest.approx(512000.0)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    port = 30500 + os.getpid() % 1000
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--config", "tiny", "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
