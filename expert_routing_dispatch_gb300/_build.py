@@ -25,8 +25,9 @@ def nvcc():
     return "nvcc"
 
 
-def _flags(verbose_ptxas=False):
+def _flags(verbose_ptxas=False, extra=()):
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
+    f += list(extra)
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
     return f
@@ -46,15 +47,19 @@ def up_to_date():
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force=False, verbose_ptxas=False, jobs=None):
-    """Compile and link libmoe.so; returns its path.  Raises on compiler errors."""
-    if not force and not verbose_ptxas and up_to_date():
+def build(force=False, verbose_ptxas=False, jobs=None, extra_flags=(), out_lib=None):
+    """Compile and link libmoe.so; returns its path.  Raises on compiler errors.
+    extra_flags / out_lib build a differently-configured copy elsewhere (tuning)."""
+    lib = out_lib or LIB
+    if not force and not verbose_ptxas and not extra_flags and out_lib is None and up_to_date():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
-    objs = [os.path.join(OUT_DIR, s.replace(".cu", ".o")) for s in SOURCES]
+    out_dir = os.path.dirname(lib)
+    os.makedirs(out_dir, exist_ok=True)
+    tag = os.path.splitext(os.path.basename(lib))[0]
+    objs = [os.path.join(out_dir, tag + "_" + s.replace(".cu", ".o")) for s in SOURCES]
 
     def compile_one(src, obj):
-        cmd = [nvcc()] + _flags(verbose_ptxas) + ["-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc()] + _flags(verbose_ptxas, extra_flags) + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, r
 
@@ -65,13 +70,13 @@ def build(force=False, verbose_ptxas=False, jobs=None):
             sys.stderr.write(r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

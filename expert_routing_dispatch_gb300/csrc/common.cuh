@@ -95,6 +95,11 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -148,17 +153,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
-// 128-byte swizzle: rows of 128 B, 8-row swizzle atoms 1024 B apart.
+// ROW-byte swizzle (ROW = 128 or 64): rows of ROW bytes, 8-row swizzle atoms
+// 8*ROW bytes apart.
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4 (unused: 1)
-//   bits 32-45 stride byte offset >> 4 (1024 B)   bits 46-47 descriptor version (1)
-//   bits 61-63 layout (2 = 128-byte swizzle)
-__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+//   bits 32-45 stride byte offset >> 4 (8*ROW)    bits 46-47 descriptor version (1)
+//   bits 61-63 layout (2 = 128-byte swizzle, 4 = 64-byte swizzle)
+template <int ROW>
+__device__ __forceinline__ uint64_t sdesc_k_swz(uint32_t saddr) {
+    static_assert(ROW == 128 || ROW == 64, "swizzle span");
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)((8 * ROW) >> 4) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)(ROW == 128 ? 2 : 4) << 61;
     return d;
 }
 

@@ -64,6 +64,7 @@ struct FusedSmem {
     int ok;
 };
 constexpr size_t FUSED_SMEM_BYTES = SMEM_BYTES + sizeof(FusedSmem);
+static_assert(FUSED_SMEM_BYTES <= 232448, "fused kernel exceeds the 227 KB shared-memory limit");
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;

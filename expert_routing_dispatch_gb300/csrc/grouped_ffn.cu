@@ -15,6 +15,7 @@ namespace moe {
 namespace {
 
 using namespace gemm;
+static_assert(SMEM_BYTES <= 232448, "grouped GEMM exceeds the 227 KB shared-memory limit");
 
 struct FfnArgs {
     const int32_t* offsets;
@@ -71,7 +72,7 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// bf16 row-major [rows, cols] matrix; box = 64 columns (128 B) x box_rows, 128-byte swizzle
+// bf16 row-major [rows, cols] matrix; box = BK columns x box_rows, swizzle span = BK * 2 bytes
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, int cols, int box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -79,8 +80,9 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, int cols, i
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle swz = (BK == 64) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

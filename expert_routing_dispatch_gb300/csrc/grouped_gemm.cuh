@@ -27,7 +27,24 @@
 namespace moe {
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+// Tile shape.  BK = 64 bf16 (128-byte rows, 128-byte swizzle) with 4 stages is the
+// default; BK = 32 (64-byte rows, 64-byte swizzle) with 8 stages keeps the same
+// ring bytes with finer refill granularity.
+#ifndef MOE_GEMM_BK
+#define MOE_GEMM_BK 64
+#endif
+#ifndef MOE_GEMM_STAGES
+#define MOE_GEMM_STAGES (256 / MOE_GEMM_BK * 1)
+#endif
+#ifndef MOE_GEMM_B_POLICY
+// weights' L2 policy: 0 evict_first, 1 evict_last, 2 evict_normal.  evict_last
+// measured best on GB300: a weight tile is read by every m-tile of its expert
+// (gate/up 1580 vs 1462 TFLOP/s on the 16384-token workload, 1126 vs 1099 at 6000)
+#define MOE_GEMM_B_POLICY 1
+#endif
+constexpr int BM = 128, BN = 256, BK = MOE_GEMM_BK, STAGES = MOE_GEMM_STAGES;
+static_assert(BK == 64 || BK == 32, "BK must be 64 (128-byte swizzle) or 32 (64-byte swizzle)");
+constexpr int ROW_BYTES = BK * 2;  // bytes of one K-row of a tile = swizzle span
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -40,6 +57,9 @@ constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
 struct Ctl {
+    // per epilogue warp: a 32-row x 128-byte staging tile (16-byte slots XOR-swizzled by
+    // row) that turns per-row TMEM reads into whole 128-byte row segments in global memory
+    alignas(128) uint4 stage[4][32 * 8];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t tfull[2];
@@ -160,7 +180,13 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
         // ================= TMA producer =================
         if (lane == 0) {
             const uint64_t pol_a = l2_policy_evict_last();
+#if MOE_GEMM_B_POLICY == 0
             const uint64_t pol_b = l2_policy_evict_first();
+#elif MOE_GEMM_B_POLICY == 1
+            const uint64_t pol_b = l2_policy_evict_last();
+#else
+            const uint64_t pol_b = l2_policy_evict_normal();
+#endif
             int e_hint = 0;
             TileCoord tc;
             bool ok = !*abort_flag;
@@ -208,8 +234,8 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = sdesc_k_sw128(a_addr(s) + kk * 32);
-                        const uint64_t bd = sdesc_k_sw128(b_addr(s) + kk * 32);
+                        const uint64_t ad = sdesc_k_swz<ROW_BYTES>(a_addr(s) + kk * 32);
+                        const uint64_t bd = sdesc_k_swz<ROW_BYTES>(b_addr(s) + kk * 32);
                         tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
                     }
                     tc_commit(smem_u32(&c.empty[s]));
@@ -227,47 +253,75 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             const int acc = p.it & 1, use = p.it >> 1;
             if (!mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status, WAIT_LIMIT)) break;
             tc_fence_after();
-            const int row_in_e = tc.mt * BM + q * 32 + lane;
-            const bool valid = row_in_e < tc.cnt;
-            const long long grow = (long long)c.row_off[tc.e] + row_in_e;
+            const int row0_in_e = tc.mt * BM + q * 32;  // first row of this warp's block
+            const long long grow0 = (long long)c.row_off[tc.e] + row0_in_e;
             const uint32_t taddr = c.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const int col0 = tc.nt * args.n_step;
+            uint4* st = c.stage[q];
             if (MODE == MODE_GATEUP) {
-                uint16_t* orow = static_cast<uint16_t*>(args.out) + grow * args.out_cols;
+                // 32 h columns per chunk: 64 B per row, 4 slots; slot = piece ^ ((row >> 1) & 3)
+                uint16_t* out = static_cast<uint16_t*>(args.out);
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 2; cc += 16) {
-                    uint32_t g[16], u[16];
-                    tmem_ld16(taddr + cc, g);
-                    tmem_ld16(taddr + BN / 2 + cc, u);
+                for (int cc = 0; cc < BN / 2; cc += 32) {
+                    uint32_t g0[16], g1[16], u0[16], u1[16];
+                    tmem_ld16(taddr + cc, g0);
+                    tmem_ld16(taddr + cc + 16, g1);
+                    tmem_ld16(taddr + BN / 2 + cc, u0);
+                    tmem_ld16(taddr + BN / 2 + cc + 16, u1);
                     tmem_ld_wait();
-                    uint32_t pk[8];
+                    uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-                        const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-                        const float h0 = g0 / (1.f + __expf(-g0)) * u0;
-                        const float h1 = g1 / (1.f + __expf(-g1)) * u1;
-                        pk[i] = pack_bf16x2(h0, h1);
+                        const float a0 = __uint_as_float(g0[2 * i]), a1 = __uint_as_float(g0[2 * i + 1]);
+                        const float b0 = __uint_as_float(u0[2 * i]), b1 = __uint_as_float(u0[2 * i + 1]);
+                        pk[i] = pack_bf16x2(a0 / (1.f + __expf(-a0)) * b0, a1 / (1.f + __expf(-a1)) * b1);
+                        const float c0 = __uint_as_float(g1[2 * i]), c1 = __uint_as_float(g1[2 * i + 1]);
+                        const float d0 = __uint_as_float(u1[2 * i]), d1 = __uint_as_float(u1[2 * i + 1]);
+                        pk[8 + i] = pack_bf16x2(c0 / (1.f + __expf(-c0)) * d0, c1 / (1.f + __expf(-c1)) * d1);
                     }
-                    if (valid && col0 + cc < args.out_cols) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + col0 + cc);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    const int sw = (lane >> 1) & 3;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        st[lane * 4 + (j ^ sw)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    __syncwarp();
+                    if (col0 + cc < args.out_cols) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = i * 8 + (lane >> 2), piece = lane & 3;
+                            const uint4 v = st[r * 4 + (piece ^ ((r >> 1) & 3))];
+                            if (row0_in_e + r < tc.cnt)
+                                *reinterpret_cast<uint4*>(out + (grow0 + r) * args.out_cols + col0 + cc + 8 * piece) = v;
+                        }
                     }
+                    __syncwarp();
                 }
             } else {
-                float* orow = static_cast<float*>(args.out) + grow * args.out_cols;
+                // 32 fp32 columns per chunk: 128 B per row, 8 slots; slot = piece ^ (row & 7)
+                float* out = static_cast<float*>(args.out);
 #pragma unroll 1
-                for (int cc = 0; cc < BN; cc += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(taddr + cc, v);
+                for (int cc = 0; cc < BN; cc += 32) {
+                    uint32_t v0[16], v1[16];
+                    tmem_ld16(taddr + cc, v0);
+                    tmem_ld16(taddr + cc + 16, v1);
                     tmem_ld_wait();
-                    if (valid && col0 + cc < args.out_cols) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + col0 + cc);
+                    const int sw = lane & 7;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    for (int j = 0; j < 4; ++j) {
+                        st[lane * 8 + (j ^ sw)] = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+                        st[lane * 8 + ((j + 4) ^ sw)] =
+                            make_uint4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
                     }
+                    __syncwarp();
+                    if (col0 + cc < args.out_cols) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int r = i * 4 + (lane >> 3), piece = lane & 7;
+                            const uint4 v = st[r * 8 + (piece ^ (r & 7))];
+                            if (row0_in_e + r < tc.cnt)
+                                *reinterpret_cast<uint4*>(out + (grow0 + r) * args.out_cols + col0 + cc + 4 * piece) = v;
+                        }
+                    }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
