@@ -96,6 +96,10 @@ def make_logits(cfg, seed=0):
     lg = normal_f32(seed, TID_LOGITS, (T, E), 0.0, cfg["logit_std"])
     if cfg.get("zipf_bias"):
         lg = (lg + zipf_bias(E)[None, :]).astype(np.float32)  # fp32 add
+    if cfg.get("one_token_per_expert"):
+        # token t's largest logit is at expert e0 + t (a margin of 64 over N(0,1) noise)
+        t = np.arange(T)
+        lg[t, cfg["e0"] + t] += np.float32(64.0)
     return lg
 
 

@@ -29,6 +29,15 @@ CONFIGS = {
                          x_std=1.0, logit_std=1.0, w_std=0.02, zipf_bias=True),
 }
 
+# "MoE GEMM" section: the decode GEMM benchmark activates every expert with a
+# single token.  One EP rank of an EP=N deployment holds n = 128/N experts and
+# sees T = n tokens, token t routed (top-1) to local expert t.
+for _ep in (1, 2, 4, 8, 16, 32):
+    _n = 128 // _ep
+    CONFIGS[f"one_token_per_expert_ep{_ep}"] = dict(
+        T=_n, H=4096, I=1536, E=128, k=1, e0=0, e1=_n, x_std=1.0, logit_std=1.0, w_std=0.02,
+        zipf_bias=False, one_token_per_expert=True)
+
 # tensor ids of the generator streams; weights are indexed by GLOBAL expert id so
 # that any local range [e0, e1) sees the same bytes as the full tensor
 TID_X, TID_LOGITS, TID_W_GATE, TID_W_UP, TID_W_DOWN = 1, 2, 3, 4, 5

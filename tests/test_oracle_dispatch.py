@@ -81,3 +81,14 @@ def test_range_slices_partition_pairs():
         seen[d["row_pair"]] += 1
         assert (d["counts"] == full["counts"][e0:e0 + 32]).all()
     assert (seen == 1).all()
+
+
+def test_one_token_per_expert_workloads():
+    """'MoE GEMM' section: every local expert receives exactly one token."""
+    for ep in (1, 8, 32):
+        cfg = synth.config(f"one_token_per_expert_ep{ep}")
+        lg = synth.make_logits(cfg)
+        st, idx, w = oracle.route(lg, cfg["k"])
+        d = oracle.dispatch(idx, cfg["e0"], cfg["e1"])
+        assert st == 0 and (d["counts"] == 1).all() and d["R"] == cfg["T"] == 128 // ep
+        assert (w == 1.0).all()
