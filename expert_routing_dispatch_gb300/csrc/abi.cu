@@ -81,7 +81,7 @@ LayerWs carve(const moe_dims* d, void* base) {
     w.pair_row = reinterpret_cast<int32_t*>(take(P * 4));
     w.x_perm = reinterpret_cast<uint16_t*>(take(P * (size_t)d->H * 2));
     w.y_perm = reinterpret_cast<float*>(take(P * (size_t)d->H * 4));
-    w.dispatch_bytes = align_up(dispatch_scratch_bytes((long long)P, (int)n));
+    w.dispatch_bytes = align_up(dispatch_scratch_bytes((long long)d->T, (int)n));
     w.dispatch_ws = take(w.dispatch_bytes);
     w.ffn_bytes = align_up(ffn_scratch_bytes((long long)P, d->I));
     w.ffn_ws = take(w.ffn_bytes);
@@ -117,7 +117,7 @@ const char* moe_status_string(int s) {
 
 size_t moe_dispatch_workspace_size(const moe_dims* d) {
     if (check_dims(d) != MOE_OK) return 0;
-    return align_up(dispatch_scratch_bytes((long long)pairs_of(d), d->e1 - d->e0));
+    return align_up(dispatch_scratch_bytes((long long)d->T, d->e1 - d->e0));
 }
 
 size_t moe_expert_ffn_workspace_size(const moe_dims* d) {
@@ -233,9 +233,14 @@ static int layer_impl(const moe_dims* d, const uint16_t* x, const float* logits,
                                            w.row_pair, w.pair_row, w.x_perm, static_cast<uint16_t*>(w.ffn_ws),
                                            w.y_perm, w.sync, d->T, d->H, d->I, d->E, d->k, d->e0, d->e1,
                                            status_dev, stall, s));
-    if (launch_route(logits, d->T, d->E, d->k, idx, wt, status_dev, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_dispatch(x, idx, d->T, d->H, d->k, d->e0, d->e1, w.counts, w.offsets, w.row_pair, w.pair_row,
-                        w.x_perm, w.dispatch_ws, s) != cudaSuccess)
+    // route also accumulates the dispatch chunk histograms; place then needs no counting pass
+    int32_t* hist = static_cast<int32_t*>(w.dispatch_ws);
+    if (cudaMemsetAsync(hist, 0, w.dispatch_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_route_hist(logits, d->T, d->E, d->k, idx, wt, status_dev, hist, dispatch_chunk_tokens(d->T), d->e0,
+                          d->e1 - d->e0, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_dispatch_place(x, idx, hist, d->T, d->H, d->k, d->e0, d->e1, w.counts, w.offsets, w.row_pair,
+                              w.pair_row, w.x_perm, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_expert_ffn(w.x_perm, w.offsets, w_gate, w_up, w_down, w.y_perm, (long long)pairs_of(d), d->H, d->I,
                           d->e1 - d->e0, w.ffn_ws, status_dev, s) != cudaSuccess)

@@ -43,17 +43,28 @@ __device__ __forceinline__ void combine_token(const float4* __restrict__ y_perm,
     __syncthreads();
     const int nr = sm.nrows;
     float4* o = out + (size_t)t * H4;
-    for (int v = threadIdx.x; v < H4; v += blockDim.x) {
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    // two output vectors per thread per pass: twice the independent loads in flight
+    for (int v0 = threadIdx.x; v0 < H4; v0 += 2 * blockDim.x) {
+        const int v1 = v0 + blockDim.x;
+        const bool has1 = v1 < H4;
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
         for (int q = 0; q < nr; ++q) {
-            const float4 y = cg ? __ldcg(y_perm + (size_t)sm.rows[q] * H4 + v) : __ldg(y_perm + (size_t)sm.rows[q] * H4 + v);
+            const float4* row = y_perm + (size_t)sm.rows[q] * H4;
+            const float4 y0 = cg ? __ldcg(row + v0) : __ldg(row + v0);
+            float4 y1 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has1) y1 = cg ? __ldcg(row + v1) : __ldg(row + v1);
             const float w = sm.wts[q];
-            a.x = fmaf(w, y.x, a.x);
-            a.y = fmaf(w, y.y, a.y);
-            a.z = fmaf(w, y.z, a.z);
-            a.w = fmaf(w, y.w, a.w);
+            a0.x = fmaf(w, y0.x, a0.x);
+            a0.y = fmaf(w, y0.y, a0.y);
+            a0.z = fmaf(w, y0.z, a0.z);
+            a0.w = fmaf(w, y0.w, a0.w);
+            a1.x = fmaf(w, y1.x, a1.x);
+            a1.y = fmaf(w, y1.y, a1.y);
+            a1.z = fmaf(w, y1.z, a1.z);
+            a1.w = fmaf(w, y1.w, a1.w);
         }
-        o[v] = a;
+        o[v0] = a0;
+        if (has1) o[v1] = a1;
     }
     __syncthreads();  // sm is reused by the next token
 }

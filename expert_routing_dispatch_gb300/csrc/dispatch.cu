@@ -8,12 +8,18 @@
 //
 // The order is fixed (a stable counting sort): rows of local expert e are
 // offsets[e] .. offsets[e+1]-1 and hold their pairs p = t*k + j in ascending p.
-// Four kernels, no host round trip:
-//   a) count   : per-CTA histogram of local experts over a chunk of 2048 pairs
-//   b) scan    : counts, exclusive offsets, and each chunk's base row per expert
-//   c) scatter : warp-ordered ranks (match_any + popc) -> row_pair, pair_row
-//   d) gather  : token-major copy of x rows into x_perm with 16-byte vectors,
-//                reading each token's row once however many local slots it has
+//
+// Main path over chunks of consecutive tokens (no host round trip):
+//   count : per-chunk histogram of local experts (moe_layer's router produces
+//           the same histogram itself, see route.cu)
+//   place : every CTA derives the offsets and its chunk's first row per expert
+//           from all chunk histograms (a redundant prefix, no scan launch), then
+//           ranks its pairs in order (match_any + popc) -> row_pair, pair_row
+//   gather: one CTA per token copies its x row into x_perm with 16-byte vectors,
+//           reading each token's row once however many local slots it has
+// The variant without a workspace (moe_dispatch_noalloc, bottom of the file)
+// runs the original four kernels: count / scan / scatter / gather over chunks of
+// 2048 pairs, with its histograms in a fixed device array.
 #include <mutex>
 
 #include "common.cuh"
@@ -156,32 +162,184 @@ __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __res
     const int nr = nrows;
     if (nr == 0) return;
     const uint4* src = x + (size_t)t * H8;
-    for (int v = threadIdx.x; v < H8; v += blockDim.x) {
-        uint4 val = __ldg(src + v);
-        for (int i = 0; i < nr; ++i) x_perm[(size_t)rows[i] * H8 + v] = val;
+    // four independent 16-byte loads in flight per thread, then the stores
+    for (int v0 = threadIdx.x; v0 < H8; v0 += 4 * blockDim.x) {
+        uint4 val[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = v0 + u * blockDim.x;
+            if (v < H8) val[u] = __ldg(src + v);
+        }
+        for (int i = 0; i < nr; ++i) {
+            uint4* dst = x_perm + (size_t)rows[i] * H8;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + u * blockDim.x;
+                if (v < H8) dst[v] = val[u];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- token chunks
+constexpr int kPlaceThreads = 256;
+constexpr int kPlaceWarps = kPlaceThreads / 32;
+
+// per-chunk histogram: chunk c = tokens [c*chunk_t, (c+1)*chunk_t)
+__global__ void __launch_bounds__(kPlaceThreads) dispatch_count_tokens_kernel(const int32_t* __restrict__ topk_idx,
+                                                                              int T, int k, int chunk_t, int e0,
+                                                                              int n, int32_t* __restrict__ hist) {
+    __shared__ int h[kMaxLocal];
+    for (int e = threadIdx.x; e < n; e += kPlaceThreads) h[e] = 0;
+    __syncthreads();
+    const long long p0 = (long long)blockIdx.x * chunk_t * k;
+    const long long p1 = (long long)min(T, (int)(blockIdx.x + 1) * chunk_t) * k;
+    for (long long p = p0 + threadIdx.x; p < p1; p += kPlaceThreads) {
+        const int e = __ldg(topk_idx + p) - e0;
+        if (e >= 0 && e < n) atomicAdd(&h[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < n; e += kPlaceThreads) hist[(size_t)blockIdx.x * n + e] = h[e];
+}
+
+__global__ void __launch_bounds__(kPlaceThreads) dispatch_place_kernel(
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ hist, int nchunks, int chunk_t, int T, int k,
+    int e0, int n, int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_pair,
+    int32_t* __restrict__ pair_row) {
+    __shared__ int tot[kMaxLocal];                // pairs of each expert, all chunks
+    __shared__ int base[kMaxLocal];               // first row of each expert for this chunk
+    __shared__ int cur[kPlaceWarps][kMaxLocal];   // per-warp counts, then per-warp cursors
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x;
+    for (int e = tid; e < n; e += kPlaceThreads) {
+        tot[e] = 0;
+        base[e] = 0;
+    }
+    for (int i = tid; i < kPlaceWarps * n; i += kPlaceThreads) cur[i / n][i % n] = 0;
+    __syncthreads();
+    // 1. totals and this chunk's prefix per expert; G threads share an expert's chunk list
+    {
+        const int G = n >= kPlaceThreads ? 1 : kPlaceThreads / n;
+        for (int i = tid; i < n * G; i += kPlaceThreads) {
+            const int e = i % n, g = i / n;
+            int t = 0, pre = 0;
+            for (int cc = g; cc < nchunks; cc += G) {
+                const int v = __ldg(hist + (size_t)cc * n + e);
+                t += v;
+                pre += (cc < c) ? v : 0;
+            }
+            if (t) atomicAdd(&tot[e], t);
+            if (pre) atomicAdd(&base[e], pre);
+        }
+    }
+    __syncthreads();
+    // 2. exclusive scan of the totals over experts (warp 0), base += offset
+    if (warp == 0) {
+        int carry = 0;
+        for (int b0 = 0; b0 < n; b0 += 32) {
+            const int e = b0 + lane;
+            const int v0 = (e < n) ? tot[e] : 0;
+            int v = v0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += y;
+            }
+            if (e < n) {
+                const int off = carry + v - v0;
+                base[e] += off;
+                if (c == 0) {
+                    counts[e] = v0;
+                    offsets[e] = off;
+                }
+            }
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (c == 0 && lane == 0) offsets[n] = carry;
+    }
+    // 3. this chunk's pairs, split into contiguous warp slices; per-warp counts
+    const int t0 = c * chunk_t, t1 = min(T, t0 + chunk_t);
+    const long long p0 = (long long)t0 * k, np = (long long)(t1 - t0) * k;
+    const long long per_warp = (np + kPlaceWarps - 1) / kPlaceWarps;
+    const long long wb = p0 + (long long)warp * per_warp, we = min(p0 + np, wb + per_warp);
+    const unsigned lt = (1u << lane) - 1u;
+    for (long long b = wb; b < we; b += 32) {
+        const long long p = b + lane;
+        const int e = (p < we) ? __ldg(topk_idx + p) - e0 : -1;
+        const bool local = e >= 0 && e < n;
+        const unsigned peers = __match_any_sync(0xffffffffu, local ? e : -1);
+        if (local && (peers & lt) == 0) cur[warp][e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = tid; e < n; e += kPlaceThreads) {  // per-warp starting rows
+        int run = base[e];
+        for (int w = 0; w < kPlaceWarps; ++w) {
+            const int cnt = cur[w][e];
+            cur[w][e] = run;
+            run += cnt;
+        }
+    }
+    __syncthreads();
+    // 4. ranks in pair order
+    for (long long b = wb; b < we; b += 32) {
+        const long long p = b + lane;
+        const bool valid = p < we;
+        const int e = valid ? __ldg(topk_idx + p) - e0 : -1;
+        const bool local = valid && e >= 0 && e < n;
+        const unsigned peers = __match_any_sync(0xffffffffu, local ? e : -1);
+        const int bse = local ? cur[warp][e] : 0;
+        __syncwarp();
+        if (local) {
+            const int row = bse + __popc(peers & lt);
+            if ((peers & lt) == 0) cur[warp][e] = bse + __popc(peers);
+            row_pair[row] = (int32_t)p;
+            pair_row[p] = row;
+        } else if (valid) {
+            pair_row[p] = -1;
+        }
+        __syncwarp();
     }
 }
 
 }  // namespace
 
-size_t dispatch_scratch_bytes(long long pairs, int n) {
-    long long nchunks = (pairs + kChunk - 1) / kChunk;
+// Chunks of at least 32 tokens, about 304 of them (two per SM of a GB300) for
+// large T.  Independent of the device, so workspace sizes are too; the result
+// does not depend on the chunking (the stable order is unique).
+int dispatch_chunk_tokens(int T) {
+    const int target = 304;
+    const int c = (T + target - 1) / target;
+    return c < 32 ? 32 : c;
+}
+
+size_t dispatch_scratch_bytes(long long T, int n) {
+    const long long chunk = dispatch_chunk_tokens((int)T);
+    const long long nchunks = (T + chunk - 1) / chunk;
     return (size_t)(nchunks * n * (long long)sizeof(int32_t));
+}
+
+cudaError_t launch_dispatch_place(const uint16_t* x, const int32_t* topk_idx, const int32_t* hist, int T, int H,
+                                  int k, int e0, int e1, int32_t* counts, int32_t* offsets, int32_t* row_pair,
+                                  int32_t* pair_row, uint16_t* x_perm, cudaStream_t s) {
+    const int chunk = dispatch_chunk_tokens(T);
+    const int nchunks = (T + chunk - 1) / chunk;
+    dispatch_place_kernel<<<nchunks, kPlaceThreads, 0, s>>>(topk_idx, hist, nchunks, chunk, T, k, e0, e1 - e0, counts,
+                                                            offsets, row_pair, pair_row);
+    // the row copy wants far more CTAs than there are chunks: one CTA per token
+    dispatch_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), T, H / 8, k, pair_row,
+                                             reinterpret_cast<uint4*>(x_perm));
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int H, int k, int e0, int e1,
                             int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
                             uint16_t* x_perm, void* scratch, cudaStream_t s) {
-    const long long P = (long long)T * k;
-    const int n = e1 - e0;
-    const int nchunks = (int)((P + kChunk - 1) / kChunk);
-    int32_t* chunk_hist = static_cast<int32_t*>(scratch);
-    dispatch_count_kernel<<<nchunks, 256, 0, s>>>(topk_idx, P, e0, n, chunk_hist);
-    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_hist, nchunks, n, counts, offsets);
-    dispatch_scatter_kernel<<<nchunks, 256, 0, s>>>(topk_idx, P, e0, n, chunk_hist, row_pair, pair_row);
-    dispatch_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), T, H / 8, k, pair_row,
-                                             reinterpret_cast<uint4*>(x_perm));
-    return cudaGetLastError();
+    const int chunk = dispatch_chunk_tokens(T);
+    const int nchunks = (T + chunk - 1) / chunk;
+    int32_t* hist = static_cast<int32_t*>(scratch);
+    dispatch_count_tokens_kernel<<<nchunks, kPlaceThreads, 0, s>>>(topk_idx, T, k, chunk, e0, e1 - e0, hist);
+    return launch_dispatch_place(x, topk_idx, hist, T, H, k, e0, e1, counts, offsets, row_pair, pair_row, x_perm, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -13,8 +13,15 @@ namespace moe {
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
                          int32_t* status, cudaStream_t s);
 
+cudaError_t launch_route_hist(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w,
+                              int32_t* status, int32_t* hist, int chunk_t, int e0, int n, cudaStream_t s);
+
 // dispatch.cu
-size_t dispatch_scratch_bytes(long long pairs, int n);
+int dispatch_chunk_tokens(int T);             // tokens per dispatch chunk
+size_t dispatch_scratch_bytes(long long T, int n);  // per-chunk histograms
+cudaError_t launch_dispatch_place(const uint16_t* x, const int32_t* topk_idx, const int32_t* hist, int T, int H,
+                                  int k, int e0, int e1, int32_t* counts, int32_t* offsets, int32_t* row_pair,
+                                  int32_t* pair_row, uint16_t* x_perm, cudaStream_t s);
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* topk_idx, int T, int H, int k, int e0, int e1,
                             int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
                             uint16_t* x_perm, void* scratch, cudaStream_t s);

@@ -32,8 +32,9 @@ __device__ __forceinline__ uint64_t route_warp_max(uint64_t v) {
 }
 
 // The whole warp routes token t.  NPL = logits per lane, E <= 32 * NPL.
+// Returns, in lane j < k, the expert of slot j (-1 in the other lanes).
 template <int NPL>
-__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
+__device__ __forceinline__ int route_token(const float* __restrict__ logits, int t, int E, int k,
                                             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                                             int32_t* status) {
     const int lane = threadIdx.x & 31;
@@ -77,6 +78,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
         topk_idx[(size_t)t * k + lane] = id;
         topk_w[(size_t)t * k + lane] = ex / sum;
     }
+    return lane < k ? id : -1;
 }
 
 // Runtime choice of the register layout for E experts (E <= 1024).
