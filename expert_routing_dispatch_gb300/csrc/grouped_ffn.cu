@@ -136,3 +136,15 @@ cudaError_t launch_expert_ffn(const uint16_t* x_perm, const int32_t* offsets, co
 }
 
 }  // namespace moe
+
+#ifdef MOE_GEMM_PROFILE
+// tuning builds only: reset / read the role wait counters of grouped_gemm.cuh
+extern "C" int moe_debug_gemm_prof(unsigned long long* host8, int reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(host8, moe::gemm::g_gemm_prof, sizeof(unsigned long long) * 8);
+    if (reset) {
+        unsigned long long z[8] = {};
+        e = cudaMemcpyToSymbol(moe::gemm::g_gemm_prof, z, sizeof(z));
+    }
+    return e == cudaSuccess ? 0 : 4;
+}
+#endif

@@ -56,6 +56,23 @@ constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
+#ifdef MOE_GEMM_PROFILE
+// Tuning builds only: clock cycles each role spends waiting, summed over CTAs.
+// [0] producer waits on a free stage   [1] producer total
+// [2] MMA waits on a free accumulator  [3] MMA waits on loaded data  [4] MMA total
+// [5] epilogue waits on an accumulator (per warp)  [6] epilogue total (per warp)  [7] tiles
+__device__ unsigned long long g_gemm_prof[8];
+#define MOE_PROF_WAIT(acc, call)                \
+    ([&]() {                                    \
+        const long long _t = clock64();         \
+        const bool _r = (call);                 \
+        acc += clock64() - _t;                  \
+        return _r;                              \
+    }())
+#else
+#define MOE_PROF_WAIT(acc, call) (call)
+#endif
+
 struct Ctl {
     // per epilogue warp: a 32-row x 128-byte staging tile (16-byte slots XOR-swizzled by
     // row) that turns per-row TMEM reads into whole 128-byte row segments in global memory
@@ -179,7 +196,16 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
-            const uint64_t pol_a = l2_policy_evict_last();
+            long long w_empty = 0, t_begin = clock64();
+            (void)w_empty;
+            (void)t_begin;
+#if defined(MOE_GEMM_A_POLICY) && MOE_GEMM_A_POLICY == 0
+            const uint64_t pol_a = l2_policy_evict_first();
+#elif defined(MOE_GEMM_A_POLICY) && MOE_GEMM_A_POLICY == 2
+            const uint64_t pol_a = l2_policy_evict_normal();
+#else
+            const uint64_t pol_a = l2_policy_evict_last();  // token rows are reread for every n-tile
+#endif
 #if MOE_GEMM_B_POLICY == 0
             const uint64_t pol_b = l2_policy_evict_first();
 #elif MOE_GEMM_B_POLICY == 1
@@ -195,7 +221,8 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                 const int b_row = tc.e * args.b_rows + tc.nt * args.n_step;
                 for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                     const int s = p.g % STAGES, r = p.g / STAGES;
-                    if (!mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag, args.status, WAIT_LIMIT)) {
+                    if (!MOE_PROF_WAIT(w_empty, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
+                                                                  args.status, WAIT_LIMIT))) {
                         ok = false;
                         break;
                     }
@@ -211,23 +238,34 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     }
                 }
             }
+#ifdef MOE_GEMM_PROFILE
+            atomicAdd(&g_gemm_prof[0], (unsigned long long)w_empty);
+            atomicAdd(&g_gemm_prof[1], (unsigned long long)(clock64() - t_begin));
+#endif
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
+            long long w_acc = 0, w_full = 0, t_begin = clock64(), ntiles = 0;
+            (void)w_acc;
+            (void)w_full;
+            (void)t_begin;
+            (void)ntiles;
             int e_hint = 0;
             TileCoord tc;
             bool ok = !*abort_flag;
             for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++p.it) {
                 const int acc = p.it & 1, use = p.it >> 1;
-                if (!mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag, args.status,
-                                       WAIT_LIMIT))
+                ++ntiles;
+                if (!MOE_PROF_WAIT(w_acc, mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag,
+                                                            args.status, WAIT_LIMIT)))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                     const int s = p.g % STAGES, r = p.g / STAGES;
-                    if (!mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status, WAIT_LIMIT)) {
+                    if (!MOE_PROF_WAIT(w_full, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status,
+                                                                 WAIT_LIMIT))) {
                         ok = false;
                         break;
                     }
@@ -243,15 +281,26 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                 if (!ok) break;
                 tc_commit(smem_u32(&c.tfull[acc]));
             }
+#ifdef MOE_GEMM_PROFILE
+            atomicAdd(&g_gemm_prof[2], (unsigned long long)w_acc);
+            atomicAdd(&g_gemm_prof[3], (unsigned long long)w_full);
+            atomicAdd(&g_gemm_prof[4], (unsigned long long)(clock64() - t_begin));
+            atomicAdd(&g_gemm_prof[7], (unsigned long long)ntiles);
+#endif
         }
     } else {
         // ================= epilogue (warps 2..5, TMEM lane quarter = warp % 4) =================
         const int q = warp & 3;
+        long long w_tf = 0, t_begin = clock64();
+        (void)w_tf;
+        (void)t_begin;
         int e_hint = 0;
         TileCoord tc;
         for (int tile = blockIdx.x; !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++p.it) {
             const int acc = p.it & 1, use = p.it >> 1;
-            if (!mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status, WAIT_LIMIT)) break;
+            if (!MOE_PROF_WAIT(w_tf, mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status,
+                                                       WAIT_LIMIT)))
+                break;
             tc_fence_after();
             const int row0_in_e = tc.mt * BM + q * 32;  // first row of this warp's block
             const long long grow0 = (long long)c.row_off[tc.e] + row0_in_e;
@@ -330,6 +379,12 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
         }
         // the stores above are read later through TMA (async proxy) by other CTAs
         asm volatile("fence.proxy.async.global;" ::: "memory");
+#ifdef MOE_GEMM_PROFILE
+        if (lane == 0) {
+            atomicAdd(&g_gemm_prof[5], (unsigned long long)w_tf);
+            atomicAdd(&g_gemm_prof[6], (unsigned long long)(clock64() - t_begin));
+        }
+#endif
     }
 }
 
