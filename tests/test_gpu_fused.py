@@ -124,3 +124,16 @@ def test_stalled_grid_barrier_reports_timeout_and_context_survives(moe):
                                         dims.e0, dims.e1)
     err, rms = rel_err(a, ref)
     assert err <= OUT_TOL * rms
+
+
+@pytest.mark.parametrize("name", ["prefill_ep_rank", "skewed"])
+def test_layer_split_path_equals_split_entries(moe, name):
+    # moe_layer above the fused threshold gathers the token rows straight from x in
+    # its gate/up GEMM; composing the public entries goes through x_perm instead
+    cfg, inp = inputs(name)
+    dims = moe.Dims.of(cfg)
+    assert dims.T * dims.k > moe.FUSED_MAX_PAIRS
+    a, ia, wa = layer(moe, dims, inp)
+    b, ib, wb = split(moe, dims, inp)
+    assert np.array_equal(ia, ib) and np.array_equal(wa.view(np.uint32), wb.view(np.uint32))
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
