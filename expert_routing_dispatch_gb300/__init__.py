@@ -12,7 +12,7 @@ import os
 
 __all__ = [
     "MoeError", "Dims", "lib", "build", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine",
-    "moe_layer", "moe_expert_gate_up", "moe_expert_down", "moe_workspace_size", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
+    "moe_layer", "moe_combine_accumulate", "moe_expert_gate_up", "moe_expert_down", "moe_workspace_size", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
     "moe_status_string", "alloc_workspace", "EXPORTED", "moe_testing_layer_stalled_barrier", "FUSED_MAX_PAIRS",
 ]
 
@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmoe.so")
 # every symbol include/moe.h declares
 EXPORTED = ("moe_status_string", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
             "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_expert_gate_up",
-            "moe_expert_down", "moe_combine", "moe_layer", "moe_testing_layer_stalled_barrier")
+            "moe_expert_down", "moe_combine", "moe_combine_accumulate", "moe_layer",
+            "moe_testing_layer_stalled_barrier")
 
 FUSED_MAX_PAIRS = 8192  # MOE_FUSED_MAX_PAIRS in include/moe.h
 
@@ -80,10 +81,11 @@ def lib():
         L.moe_expert_gate_up.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_down.argtypes = [pd, vp, vp, vp, vp, vp, vp]
         L.moe_combine.argtypes = [pd, vp, vp, vp, vp, vp]
+        L.moe_combine_accumulate.argtypes = [pd, vp, vp, vp, vp, vp]
         L.moe_layer.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         L.moe_testing_layer_stalled_barrier.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         for f in (L.moe_route, L.moe_dispatch, L.moe_dispatch_noalloc, L.moe_expert_ffn, L.moe_expert_gate_up, L.moe_expert_down,
-                  L.moe_combine, L.moe_layer, L.moe_testing_layer_stalled_barrier):
+                  L.moe_combine, L.moe_combine_accumulate, L.moe_layer, L.moe_testing_layer_stalled_barrier):
             f.restype = i32
         _lib = L
     return _lib
@@ -189,6 +191,12 @@ def moe_combine(dims, y_perm, pair_row, topk_w, out, stream=None):
     d = Dims.of(dims)
     _check(lib().moe_combine(ctypes.byref(d), _ptr(y_perm), _ptr(pair_row), _ptr(topk_w), _ptr(out), _stream(stream)),
            "moe_combine")
+
+
+def moe_combine_accumulate(dims, y_perm, pair_row, topk_w, out, stream=None):
+    d = Dims.of(dims)
+    _check(lib().moe_combine_accumulate(ctypes.byref(d), _ptr(y_perm), _ptr(pair_row), _ptr(topk_w), _ptr(out),
+                                        _stream(stream)), "moe_combine_accumulate")
 
 
 def moe_layer(dims, x, logits, w_gate, w_up, w_down, out, ws, ws_bytes=None, topk_idx=None, topk_w=None,

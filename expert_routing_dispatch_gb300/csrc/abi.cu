@@ -209,6 +209,15 @@ int moe_combine(const moe_dims* d, const float* y_perm, const int32_t* pair_row,
     return launched(launch_combine(y_perm, pair_row, topk_w, d->T, d->H, d->k, out, (cudaStream_t)stream));
 }
 
+int moe_combine_accumulate(const moe_dims* d, const float* y_perm, const int32_t* pair_row, const float* topk_w,
+                           float* out, void* stream) {
+    int st = check_dims(d);
+    if (st) return st;
+    if (!aligned16(y_perm) || !aligned16(pair_row) || !aligned16(topk_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if ((st = check_device())) return st;
+    return launched(launch_combine(y_perm, pair_row, topk_w, d->T, d->H, d->k, out, (cudaStream_t)stream, true));
+}
+
 static int layer_impl(const moe_dims* d, const uint16_t* x, const float* logits, const uint16_t* w_gate,
                       const uint16_t* w_up, const uint16_t* w_down, float* out, int32_t* topk_idx_opt,
                       float* topk_w_opt, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream, int stall) {

@@ -20,10 +20,11 @@ struct CombineSmem {
 };
 
 // The whole CTA (nthreads threads) combines token t.  `cg` selects L2-coherent
-// loads for indices written earlier in the same launch by other CTAs.
+// loads for indices written earlier in the same launch by other CTAs.  With
+// `accumulate` the sum starts from the current out[t] instead of zero.
 __device__ __forceinline__ void combine_token(const float4* __restrict__ y_perm, const int32_t* pair_row,
                                               const float* topk_w, int t, int H4, int k, float4* __restrict__ out,
-                                              CombineSmem& sm, bool cg) {
+                                              CombineSmem& sm, bool cg, bool accumulate = false) {
     if (threadIdx.x < 32) {
         const int j = threadIdx.x;
         int r = -1;
@@ -48,6 +49,10 @@ __device__ __forceinline__ void combine_token(const float4* __restrict__ y_perm,
         const int v1 = v0 + blockDim.x;
         const bool has1 = v1 < H4;
         float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+        if (accumulate) {
+            a0 = o[v0];
+            if (has1) a1 = o[v1];
+        }
         for (int q = 0; q < nr; ++q) {
             const float4* row = y_perm + (size_t)sm.rows[q] * H4;
             const float4 y0 = cg ? __ldcg(row + v0) : __ldg(row + v0);

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) {
         build_tile_table(c, n, (a.I + BN / 2 - 1) / (BN / 2));
         __syncthreads();
-        const Args ga{a.h, a.status, n, a.H / BK, (a.I + BN / 2 - 1) / (BN / 2), a.I, a.I, BN / 2};
+        const Args ga{a.h, a.status, n, a.H / BK, (a.I + BN / 2 - 1) / (BN / 2), a.I, a.I, BN / 2, 0};
         run_phase<MODE_GATEUP>(c, ring, p, &tmX, &tmG, &tmU, ga);
         ok = grid_sync(a, 3u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) {
         build_tile_table(c, n, (a.H + BN - 1) / BN);
         __syncthreads();
-        const Args da{a.y_perm, a.status, n, a.I / BK, (a.H + BN - 1) / BN, a.H, a.H, BN};
+        const Args da{a.y_perm, a.status, n, a.I / BK, (a.H + BN - 1) / BN, a.H, a.H, BN, 0};  // no prefetch: measured slower here
         run_phase<MODE_DOWN>(c, ring, p, &tmH, &tmD, &tmD, da);
         ok = grid_sync(a, 4u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }

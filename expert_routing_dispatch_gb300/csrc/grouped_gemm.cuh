@@ -98,6 +98,7 @@ struct Args {
     int out_cols;     // I (gate/up) or H (down)
     int b_rows;       // weight rows per expert in the B tensor map (I or H)
     int n_step;       // output columns per n-tile (128 or 256)
+    int prefetch;     // L2 prefetch distance of the weight boxes in k-blocks (0 = off)
 };
 
 // Per-thread pipeline counters; they carry over from one GEMM phase to the next
@@ -225,6 +226,14 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                                                                   args.status, WAIT_LIMIT))) {
                         ok = false;
                         break;
+                    }
+                    // The first m-tile of each weight tile pulls the weight boxes PF k-blocks
+                    // ahead into L2 (only boxes wholly inside the tensor).
+                    const int PF = args.prefetch;
+                    if (PF > 0 && tc.mt == 0 && kb + PF < args.kblocks &&
+                        b_row + (MODE == MODE_GATEUP ? BN / 2 : BN) <= n * args.b_rows) {
+                        tma_prefetch_l2_2d(tmB0, (kb + PF) * BK, b_row);
+                        if (MODE == MODE_GATEUP) tma_prefetch_l2_2d(tmB1, (kb + PF) * BK, b_row);
                     }
                     const uint32_t fb = smem_u32(&c.full[s]);
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);

@@ -35,7 +35,7 @@ cudaError_t launch_dispatch_noalloc(const uint16_t* x, const int32_t* topk_idx, 
 
 // combine.cu
 cudaError_t launch_combine(const float* y_perm, const int32_t* pair_row, const float* topk_w, int T, int H, int k,
-                           float* out, cudaStream_t s);
+                           float* out, cudaStream_t s, bool accumulate = false);
 
 // grouped_ffn.cu
 size_t ffn_scratch_bytes(long long rows, int I);

@@ -168,6 +168,17 @@ int moe_expert_down(const moe_dims* d, const uint16_t* h, const int32_t* offsets
 int moe_combine(const moe_dims* d, const float* y_perm, const int32_t* pair_row,
                 const float* topk_w, float* out, void* stream);
 
+/*
+ * Combine that adds into `out` instead of overwriting it: out[t] += the same
+ * slot-ordered fp32 sum.  "Data Parallel and Expert Parallel" section: the DP-EP
+ * kernel returns each expert's results to the tokens' source rank and
+ * accumulates them there; with several expert ranges (or token shards) on one
+ * GPU, each range's combine accumulates into one output buffer.  Arguments as
+ * for moe_combine; out must hold the running sum (e.g. zeros) on entry.
+ */
+int moe_combine_accumulate(const moe_dims* d, const float* y_perm, const int32_t* pair_row,
+                           const float* topk_w, float* out, void* stream);
+
 /* T*k at or below which moe_layer runs the fused single-launch (decode) path. */
 #define MOE_FUSED_MAX_PAIRS 8192
 
