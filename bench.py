@@ -31,8 +31,12 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer routed tokens/s + TFLOP/s (prefill), weight GB/s (decode), 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["expert_routing_dispatch_gb300/csrc/grouped_ffn.cu", "expert_routing_dispatch_gb300/csrc/grouped_gemm.cuh",
-                  "expert_routing_dispatch_gb300/csrc/common.cuh"]
+_CS = "expert_routing_dispatch_gb300/csrc/"
+KERNEL_SOURCES = {
+    "grouped_gemm_gate_up": [_CS + "grouped_ffn.cu", _CS + "grouped_gemm.cuh", _CS + "common.cuh"],
+    "moe_layer_fused": [_CS + "decode_fused.cu", _CS + "grouped_gemm.cuh", _CS + "common.cuh", _CS + "route.cuh",
+                        _CS + "combine.cuh"],
+}
 
 
 def parse():
@@ -81,18 +85,18 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0), "fallback"
 
 
-def kernel_hash():
+def kernel_hash(kernel):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config):
-    """DRAM bytes per gate/up launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"grouped_gemm_gate_up.{config}.md")
+def recorded_traffic(kernel, config):
+    """DRAM bytes per launch of `kernel` on `config` from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.{config}.md")
     try:
         lines = open(path).read().splitlines()
     except OSError:
@@ -103,7 +107,7 @@ def recorded_traffic(config):
             k, v = ln[2:].split(":", 1)
             kv[k.strip()] = v.strip().strip("`")
     try:
-        if kv.get("kernel_source_sha256_16") != kernel_hash():
+        if kv.get("kernel_source_sha256_16") != kernel_hash(kernel):
             return None
         return float(kv["dram_bytes_per_launch_full_size"])
     except (KeyError, ValueError):
@@ -391,13 +395,15 @@ def run_ours(args):
         roofline = {"kernel": "moe_layer_fused_kernel (route..combine, one cooperative launch)", "bound": "hbm",
                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
-                    "traffic": None, "algorithmic_bytes_per_launch": alg_bytes}
+                    "traffic": recorded_traffic("moe_layer_fused", args.config),
+                    "algorithmic_bytes_per_launch": alg_bytes}
     else:
         achieved = flop_gate_up / (kern_ms["gate_up"] * 1e-3) / 1e12 if R else 0.0
         roofline = {"kernel": "grouped_ffn gate/up (tcgen05, SiLU*up epilogue)", "bound": "tensor",
                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
-                    "traffic": recorded_traffic(args.config), "algorithmic_flop_per_launch": flop_gate_up}
+                    "traffic": recorded_traffic("grouped_gemm_gate_up", args.config),
+                    "algorithmic_flop_per_launch": flop_gate_up}
     gemm_ms = kern_ms["layer_fused"] if fused else kern_ms["gate_up"] + kern_ms["down"]
     line = {
         "metric": METRIC,
