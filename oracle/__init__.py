@@ -33,27 +33,31 @@ def build(force=False):
     return _SO
 
 
+def _bind(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.oracle_route.argtypes = [i64, i32, i32, vp, vp, vp]
+    lib.oracle_route.restype = i32
+    lib.oracle_dispatch.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.oracle_dispatch.restype = i64
+    lib.oracle_expert_ffn_rows.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp]
+    lib.oracle_expert_ffn_rows.restype = None
+    lib.oracle_expert_ffn_rowlist.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp]
+    lib.oracle_expert_ffn_rowlist.restype = None
+    lib.oracle_combine_tokens.argtypes = [i32, i32, vp, vp, vp, vp, i64, vp]
+    lib.oracle_combine_tokens.restype = None
+    lib.oracle_moe_layer_tokens.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp]
+    lib.oracle_moe_layer_tokens.restype = i32
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i32
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_SO)
-        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-        lib.oracle_route.argtypes = [i64, i32, i32, vp, vp, vp]
-        lib.oracle_route.restype = i32
-        lib.oracle_dispatch.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp]
-        lib.oracle_dispatch.restype = i64
-        lib.oracle_expert_ffn_rows.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp]
-        lib.oracle_expert_ffn_rows.restype = None
-        lib.oracle_expert_ffn_rowlist.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp]
-        lib.oracle_expert_ffn_rowlist.restype = None
-        lib.oracle_combine_tokens.argtypes = [i32, i32, vp, vp, vp, vp, i64, vp]
-        lib.oracle_combine_tokens.restype = None
-        lib.oracle_moe_layer_tokens.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp]
-        lib.oracle_moe_layer_tokens.restype = i32
-        lib.oracle_num_threads.argtypes = []
-        lib.oracle_num_threads.restype = i32
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(_SO))
     return _lib
 
 

@@ -1,0 +1,85 @@
+"""The pins are strong enough to catch plausible mistakes: each mistake below is
+planted in a copy of oracle.c (on the CPU, in a temporary directory), the copy is
+built and swapped in for the oracle, and at least one pin must then fail.  The
+unmodified oracle passes the same pins (the first case)."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_dispatch as pd
+import test_oracle_ffn_combine as pf
+import test_oracle_route as pr
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# name -> (text in oracle.c, planted replacement)
+MUTANTS = {
+    "none": None,
+    "ties_to_higher_id": ("if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] >= l[best]) best = e;"),
+    "weights_not_renormalised": ("w[j] = exp((double)l[idx[j]] - m) / s;", "w[j] = exp((double)l[idx[j]] - m);"),
+    "silu_sign": ("double silu = g / (1.0 + exp(-g));", "double silu = g / (1.0 + exp(g));"),
+    "gate_and_up_swapped": ("double silu = g / (1.0 + exp(-g));\n        act[i] = silu * u;",
+                            "double silu = u / (1.0 + exp(-u));\n        act[i] = silu * g;"),
+    "down_weights_transposed": ("acc += bf16_widen(rd[i]) * act[i];",
+                                "acc += bf16_widen(wd[(int64_t)i * H + h]) * act[i];"),
+    "dispatch_rows_descending": ("int32_t r = offsets[e - e0] + fill[e - e0]++;",
+                                 "int32_t r = offsets[e - e0 + 1] - 1 - fill[e - e0]++;"),
+    "combine_ignores_weights": ("o[h] += w * (double)y_perm[(int64_t)r * H + h];",
+                                "o[h] += (double)y_perm[(int64_t)r * H + h];"),
+    "layer_ignores_weights": ("for (int h = 0; h < H; ++h) o[h] += w[j] * y[h];",
+                              "for (int h = 0; h < H; ++h) o[h] += y[h];"),
+}
+
+PINS = [
+    lambda: pr.test_selection_matches_full_sort(16, 4),
+    lambda: pr.test_signed_zero_ties_to_lower_id(),
+    lambda: pr.test_hand_worked_example(),
+    lambda: pr.test_two_expert_closed_form(),
+    lambda: pr.test_weights_equal_renormalised_full_softmax(),
+    lambda: pd.test_dispatch_invariants(16, 4, 3, 11),
+    lambda: pf.test_single_expert_is_textbook_mlp(),
+    lambda: pf.test_identity_weights_closed_form(),
+    lambda: pf.test_dense_masked_formula(0, 6),
+    lambda: pf.test_grouped_rows_match_textbook(),
+    lambda: pf.test_combine_is_slot_ordered_weighted_gather(),
+]
+
+
+def build_variant(tmp_path, name):
+    src = open(SRC).read()
+    if MUTANTS[name] is not None:
+        old, new = MUTANTS[name]
+        assert src.count(old) == 1, f"mutation site of {name} not found once in oracle.c"
+        src = src.replace(old, new)
+    c = tmp_path / f"oracle_{name}.c"
+    so = tmp_path / f"liboracle_{name}.so"
+    c.write_text(src)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", str(c), "-o", str(so), "-lm"], check=True)
+    return oracle._bind(ctypes.CDLL(str(so)))
+
+
+def failing_pins(lib):
+    saved = oracle._load()
+    oracle._lib = lib
+    failed = 0
+    try:
+        for pin in PINS:
+            try:
+                pin()
+            except AssertionError:
+                failed += 1
+    finally:
+        oracle._lib = saved
+    return failed
+
+
+@pytest.mark.parametrize("name", list(MUTANTS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    failed = failing_pins(build_variant(tmp_path, name))
+    if name == "none":
+        assert failed == 0
+    else:
+        assert failed >= 1, f"no pin caught the planted mistake {name}"
