@@ -36,6 +36,7 @@ namespace {
 using namespace gemm;
 
 constexpr long long GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles
+constexpr int SMALL_ROWS = 32;                    // rows of the small token-tile boxes
 
 struct FusedArgs {
     const float* logits;
@@ -53,6 +54,7 @@ struct FusedArgs {
     unsigned* sync;
     int32_t* status;
     int T, H, I, E, k, e0, e1;
+    int bn;     // MMA N (weight rows per GEMM tile): 256, or 128 when there are few local experts
     int stall;  // testing hook: extra arrivals the first barrier waits for (0 in normal use)
 };
 
@@ -106,7 +108,10 @@ __device__ bool grid_sync(const FusedArgs& a, unsigned target, FusedSmem& fs) {
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     moe_layer_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                            const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
-                           const __grid_constant__ CUtensorMap tmD, const FusedArgs a) {
+                           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmXs,
+                           const __grid_constant__ CUtensorMap tmHs, const FusedArgs a) {
+    // tmXs / tmHs: x_perm / h with SMALL_ROWS-row boxes, for m-tiles with that few rows
+    // (decode has ~16 tokens per expert: 4x less token-tile traffic than 128-row boxes)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t ring = ring_base(smem_raw);
     Ctl& c = ctl_of(smem_raw);
@@ -123,6 +128,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmU);
         tma_prefetch_desc(&tmH);
         tma_prefetch_desc(&tmD);
+        tma_prefetch_desc(&tmXs);
+        tma_prefetch_desc(&tmHs);
     }
     tc_fence_before();
     __syncthreads();
@@ -229,19 +236,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // ---------------- P2: gate/up GEMM + SiLU*up
     if (ok) {
-        build_tile_table(c, n, (a.I + BN / 2 - 1) / (BN / 2));
+        const Args ga{a.h, a.status, n, a.H / BK, (a.I + a.bn / 2 - 1) / (a.bn / 2), a.I, a.I, a.bn / 2, 0, a.bn,
+                      SMALL_ROWS};
+        build_tile_table(c, n, ga.ntiles_n);
         __syncthreads();
-        const Args ga{a.h, a.status, n, a.H / BK, (a.I + BN / 2 - 1) / (BN / 2), a.I, a.I, BN / 2, 0};
-        run_phase<MODE_GATEUP>(c, ring, p, &tmX, &tmG, &tmU, ga);
+        run_phase<MODE_GATEUP>(c, ring, p, &tmX, &tmG, &tmU, ga, &tmXs);
         ok = grid_sync(a, 3u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }
 
     // ---------------- P3: down GEMM
     if (ok) {
-        build_tile_table(c, n, (a.H + BN - 1) / BN);
+        // no weight prefetch here: measured slower in this launch
+        const Args da{a.y_perm, a.status, n, a.I / BK, (a.H + a.bn - 1) / a.bn, a.H, a.H, a.bn, 0, a.bn, SMALL_ROWS};
+        build_tile_table(c, n, da.ntiles_n);
         __syncthreads();
-        const Args da{a.y_perm, a.status, n, a.I / BK, (a.H + BN - 1) / BN, a.H, a.H, BN, 0};  // no prefetch: measured slower here
-        run_phase<MODE_DOWN>(c, ring, p, &tmH, &tmD, &tmD, da);
+        run_phase<MODE_DOWN>(c, ring, p, &tmH, &tmD, &tmD, da, &tmHs);
         ok = grid_sync(a, 4u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }
 
@@ -270,18 +279,23 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     if (attr != cudaSuccess) return attr;
     const int n = e1 - e0;
     const long long rows = (long long)T * k;
-    CUtensorMap mX, mG, mU, mH, mD;
-    if (!make_tmap_bf16(&mX, x_perm, rows, H, BM) || !make_tmap_bf16(&mG, w_gate, (long long)n * I, H, BN / 2) ||
-        !make_tmap_bf16(&mU, w_up, (long long)n * I, H, BN / 2) || !make_tmap_bf16(&mH, h, rows, I, BM) ||
-        !make_tmap_bf16(&mD, w_down, (long long)n * H, I, BN))
+    // 256-row weight tiles.  (128-row tiles for few local experts measured slower:
+    // each tile then reloads its token tile for half the work.)
+    const int grid = sm_count();
+    const int bn = BN;
+    CUtensorMap mX, mG, mU, mH, mD, mXs, mHs;
+    if (!make_tmap_bf16(&mXs, x_perm, rows, H, SMALL_ROWS) || !make_tmap_bf16(&mHs, h, rows, I, SMALL_ROWS) ||
+        !make_tmap_bf16(&mX, x_perm, rows, H, BM) || !make_tmap_bf16(&mG, w_gate, (long long)n * I, H, bn / 2) ||
+        !make_tmap_bf16(&mU, w_up, (long long)n * I, H, bn / 2) || !make_tmap_bf16(&mH, h, rows, I, BM) ||
+        !make_tmap_bf16(&mD, w_down, (long long)n * H, I, bn))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
     FusedArgs a{logits, reinterpret_cast<const uint4*>(x), topk_idx, topk_w, counts, offsets, row_pair, pair_row,
-                reinterpret_cast<uint4*>(x_perm), h, y_perm, out, sync, status, T, H, I, E, k, e0, e1,
+                reinterpret_cast<uint4*>(x_perm), h, y_perm, out, sync, status, T, H, I, E, k, e0, e1, bn,
                 stall_first_barrier};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sm_count());
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = FUSED_SMEM_BYTES;
     cfg.stream = s;
@@ -290,7 +304,7 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_layer_fused_kernel, mX, mG, mU, mH, mD, a);
+    return cudaLaunchKernelEx(&cfg, moe_layer_fused_kernel, mX, mG, mU, mH, mD, mXs, mHs, a);
 }
 
 }  // namespace moe

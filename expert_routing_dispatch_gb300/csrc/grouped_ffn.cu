@@ -115,7 +115,7 @@ cudaError_t launch_gate_up(const uint16_t* x_perm, const int32_t* offsets, const
     if (!make_tmap_bf16(&mA, x_perm, rows, H, BM) || !make_tmap_bf16(&mG, w_gate, (long long)n * I, H, BN / 2) ||
         !make_tmap_bf16(&mU, w_up, (long long)n * I, H, BN / 2))
         return cudaErrorInvalidValue;
-    FfnArgs a{offsets, {h, status, n, H / BK, (I + BN / 2 - 1) / (BN / 2), I, I, BN / 2, kPrefetchGateUp}};
+    FfnArgs a{offsets, {h, status, n, H / BK, (I + BN / 2 - 1) / (BN / 2), I, I, BN / 2, kPrefetchGateUp, BN, 0}};
     grouped_ffn_kernel<MODE_GATEUP><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mA, mG, mU, a);
     return cudaGetLastError();
 }
@@ -127,7 +127,7 @@ cudaError_t launch_down(const uint16_t* h, const int32_t* offsets, const uint16_
     CUtensorMap mH, mD;
     if (!make_tmap_bf16(&mH, h, rows, I, BM) || !make_tmap_bf16(&mD, w_down, (long long)n * H, I, BN))
         return cudaErrorInvalidValue;
-    FfnArgs a{offsets, {y_perm, status, n, I / BK, (H + BN - 1) / BN, H, H, BN, kPrefetchDown}};
+    FfnArgs a{offsets, {y_perm, status, n, I / BK, (H + BN - 1) / BN, H, H, BN, kPrefetchDown, BN, 0}};
     grouped_ffn_kernel<MODE_DOWN><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mH, mD, mD, a);
     return cudaGetLastError();
 }

@@ -52,7 +52,6 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_LOCAL = 1024;
 constexpr long long WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
@@ -97,8 +96,10 @@ struct Args {
     int ntiles_n;     // n-tiles per expert
     int out_cols;     // I (gate/up) or H (down)
     int b_rows;       // weight rows per expert in the B tensor map (I or H)
-    int n_step;       // output columns per n-tile (128 or 256)
+    int n_step;       // output columns per n-tile (bn / 2 for gate/up, bn for down)
     int prefetch;     // L2 prefetch distance of the weight boxes in k-blocks (0 = off)
+    int bn;           // MMA N = weight rows per tile (256; 128 also supported)
+    int a_small;      // box rows of the optional small token map (0 = none)
 };
 
 // Per-thread pipeline counters; they carry over from one GEMM phase to the next
@@ -185,9 +186,13 @@ __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_
 }
 
 // One GEMM phase, every thread of the CTA calls it and plays its role.
+//   tmA_small (optional): the same token matrix with args.a_small-row boxes.  An
+//   m-tile with at most a_small valid rows loads only those rows; the MMA still
+//   reads 128 rows, and the stale ones only feed output rows that are not stored.
 template <int MODE>
 __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const CUtensorMap* tmA,
-                                          const CUtensorMap* tmB0, const CUtensorMap* tmB1, const Args& args) {
+                                          const CUtensorMap* tmB0, const CUtensorMap* tmB1, const Args& args,
+                                          const CUtensorMap* tmA_small = nullptr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = args.n;
     volatile int* abort_flag = &c.abort_flag;
@@ -220,6 +225,9 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
                 const int a_row = c.row_off[tc.e] + tc.mt * BM;
                 const int b_row = tc.e * args.b_rows + tc.nt * args.n_step;
+                const bool a_small = tmA_small != nullptr && tc.cnt - tc.mt * BM <= args.a_small;
+                const CUtensorMap* tma_a = a_small ? tmA_small : tmA;
+                const uint32_t stage_tx = (uint32_t)((a_small ? args.a_small : BM) * BK * 2 + args.bn * BK * 2);
                 for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                     const int s = p.g % STAGES, r = p.g / STAGES;
                     if (!MOE_PROF_WAIT(w_empty, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
@@ -231,17 +239,17 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     // ahead into L2 (only boxes wholly inside the tensor).
                     const int PF = args.prefetch;
                     if (PF > 0 && tc.mt == 0 && kb + PF < args.kblocks &&
-                        b_row + (MODE == MODE_GATEUP ? BN / 2 : BN) <= n * args.b_rows) {
+                        b_row + (MODE == MODE_GATEUP ? args.bn / 2 : args.bn) <= n * args.b_rows) {
                         tma_prefetch_l2_2d(tmB0, (kb + PF) * BK, b_row);
                         if (MODE == MODE_GATEUP) tma_prefetch_l2_2d(tmB1, (kb + PF) * BK, b_row);
                     }
                     const uint32_t fb = smem_u32(&c.full[s]);
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    mbar_arrive_expect_tx(fb, stage_tx);
                     p.issued[s] = r + 1;
-                    tma_load_2d(a_addr(s), tmA, kb * BK, a_row, fb, pol_a);
-                    if (MODE == MODE_GATEUP) {
+                    tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
+                    if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn/2 each
                         tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
-                        tma_load_2d(b_addr(s) + B_BYTES / 2, tmB1, kb * BK, b_row, fb, pol_b);
+                        tma_load_2d(b_addr(s) + (uint32_t)(args.bn / 2) * BK * 2, tmB1, kb * BK, b_row, fb, pol_b);
                     } else {
                         tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
                     }
@@ -271,6 +279,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * BN);
+                const uint32_t idesc = idesc_bf16_f32(BM, args.bn);
                 for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                     const int s = p.g % STAGES, r = p.g / STAGES;
                     if (!MOE_PROF_WAIT(w_full, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status,
@@ -283,7 +292,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t ad = sdesc_k_swz<ROW_BYTES>(a_addr(s) + kk * 32);
                         const uint64_t bd = sdesc_k_swz<ROW_BYTES>(b_addr(s) + kk * 32);
-                        tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+                        tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                     }
                     tc_commit(smem_u32(&c.empty[s]));
                 }
@@ -320,12 +329,12 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                 // 32 h columns per chunk: 64 B per row, 4 slots; slot = piece ^ ((row >> 1) & 3)
                 uint16_t* out = static_cast<uint16_t*>(args.out);
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 2; cc += 32) {
+                for (int cc = 0; cc < args.bn / 2; cc += 32) {
                     uint32_t g0[16], g1[16], u0[16], u1[16];
                     tmem_ld16(taddr + cc, g0);
                     tmem_ld16(taddr + cc + 16, g1);
-                    tmem_ld16(taddr + BN / 2 + cc, u0);
-                    tmem_ld16(taddr + BN / 2 + cc + 16, u1);
+                    tmem_ld16(taddr + args.bn / 2 + cc, u0);
+                    tmem_ld16(taddr + args.bn / 2 + cc + 16, u1);
                     tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
@@ -357,7 +366,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                 // 32 fp32 columns per chunk: 128 B per row, 8 slots; slot = piece ^ (row & 7)
                 float* out = static_cast<float*>(args.out);
 #pragma unroll 1
-                for (int cc = 0; cc < BN; cc += 32) {
+                for (int cc = 0; cc < args.bn; cc += 32) {
                     uint32_t v0[16], v1[16];
                     tmem_ld16(taddr + cc, v0);
                     tmem_ld16(taddr + cc + 16, v1);
