@@ -223,10 +223,20 @@ __global__ void __launch_bounds__(kPlaceThreads) dispatch_place_kernel(
         for (int i = tid; i < n * G; i += kPlaceThreads) {
             const int e = i % n, g = i / n;
             int t = 0, pre = 0;
-            for (int cc = g; cc < nchunks; cc += G) {
-                const int v = __ldg(hist + (size_t)cc * n + e);
-                t += v;
-                pre += (cc < c) ? v : 0;
+            // eight independent loads in flight per pass (a dependent chain of L2
+            // loads made this loop the kernel's critical path)
+            for (int cb = g; cb < nchunks; cb += 8 * G) {
+                int v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int cc = cb + u * G;
+                    v[u] = cc < nchunks ? __ldg(hist + (size_t)cc * n + e) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    t += v[u];
+                    pre += (cb + u * G < c) ? v[u] : 0;
+                }
             }
             if (t) atomicAdd(&tot[e], t);
             if (pre) atomicAdd(&base[e], pre);
