@@ -44,32 +44,38 @@ __device__ __forceinline__ void combine_token(const float4* __restrict__ y_perm,
     __syncthreads();
     const int nr = sm.nrows;
     float4* o = out + (size_t)t * H4;
-    // two output vectors per thread per pass: twice the independent loads in flight
-    for (int v0 = threadIdx.x; v0 < H4; v0 += 2 * blockDim.x) {
-        const int v1 = v0 + blockDim.x;
-        const bool has1 = v1 < H4;
-        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-        if (accumulate) {
-            a0 = o[v0];
-            if (has1) a1 = o[v1];
+    // four output vectors per thread per pass: four independent 16-byte loads of
+    // every row in flight (the per-element fma chain is in slot order either way)
+    constexpr int U = 4;
+    const int bd = blockDim.x;
+    for (int v0 = threadIdx.x; v0 < H4; v0 += U * bd) {
+        float4 a[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (accumulate && v0 + u * bd < H4) a[u] = o[v0 + u * bd];
         }
         for (int q = 0; q < nr; ++q) {
             const float4* row = y_perm + (size_t)sm.rows[q] * H4;
-            const float4 y0 = cg ? __ldcg(row + v0) : __ldg(row + v0);
-            float4 y1 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has1) y1 = cg ? __ldcg(row + v1) : __ldg(row + v1);
             const float w = sm.wts[q];
-            a0.x = fmaf(w, y0.x, a0.x);
-            a0.y = fmaf(w, y0.y, a0.y);
-            a0.z = fmaf(w, y0.z, a0.z);
-            a0.w = fmaf(w, y0.w, a0.w);
-            a1.x = fmaf(w, y1.x, a1.x);
-            a1.y = fmaf(w, y1.y, a1.y);
-            a1.z = fmaf(w, y1.z, a1.z);
-            a1.w = fmaf(w, y1.w, a1.w);
+            float4 y[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * bd;
+                y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (v < H4) y[u] = cg ? __ldcg(row + v) : __ldg(row + v);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                a[u].x = fmaf(w, y[u].x, a[u].x);
+                a[u].y = fmaf(w, y[u].y, a[u].y);
+                a[u].z = fmaf(w, y[u].z, a[u].z);
+                a[u].w = fmaf(w, y[u].w, a[u].w);
+            }
         }
-        o[v0] = a0;
-        if (has1) o[v1] = a1;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v0 + u * bd < H4) o[v0 + u * bd] = a[u];
     }
     __syncthreads();  // sm is reused by the next token
 }

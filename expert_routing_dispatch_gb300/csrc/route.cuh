@@ -6,10 +6,11 @@
 // order, ties to the lower expert id; weights = softmax over the k picks (equal
 // to the full softmax renormalised over them).
 //
-// Selection is exact: each (logit, id) maps to a 64-bit key whose unsigned order
-// is "larger logit first, then lower id" (-0.0 folded onto +0.0), so each of the
-// k passes is a plain warp max over keys.  Lane l holds the logits of experts
-// l, l+32, l+64, ... in registers (coalesced loads).
+// Selection is exact: each logit maps to 32 bits whose unsigned order is the
+// float order (-0.0 folded onto +0.0).  Each of the k passes takes the warp
+// maximum of those bits (redux.sync), then the lowest expert id holding it (a
+// second redux.sync), so ties go to the lower id.  Lane l holds the logits of
+// experts l, l+32, l+64, ... in registers (coalesced loads).
 #pragma once
 
 #include "common.cuh"
@@ -22,15 +23,6 @@ __device__ __forceinline__ uint32_t route_ordered_bits(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ uint64_t route_warp_max(uint64_t v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = w > v ? w : v;
-    }
-    return v;
-}
-
 // The whole warp routes token t.  NPL = logits per lane, E <= 32 * NPL.
 // Returns, in lane j < k, the expert of slot j (-1 in the other lanes).
 template <int NPL>
@@ -39,37 +31,40 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, int
                                             int32_t* status) {
     const int lane = threadIdx.x & 31;
     const float* row = logits + (size_t)t * E;
-    uint64_t key[NPL];
+    uint32_t key[NPL];  // ordered bits, 0 = removed or absent
     bool finite = true;
 #pragma unroll
     for (int c = 0; c < NPL; ++c) {
         const int e = c * 32 + lane;
+        key[c] = 0;
         if (e < E) {
             const float v = __ldg(row + e);
             finite &= isfinite(v);
-            key[c] = ((uint64_t)route_ordered_bits(v) << 32) | (uint32_t)(0xffffffffu - (uint32_t)e);
-        } else {
-            key[c] = 0;  // below every real key
+            key[c] = max(route_ordered_bits(v), 1u);  // 0 only for a NaN pattern, which is flagged below
         }
     }
     if (__any_sync(0xffffffffu, !finite) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
 
-    // k passes of warp argmax; lane j keeps the j-th pick
-    uint64_t mine = 0;
+    // k passes: warp max of the bits, then the lowest id holding it; lane j keeps pick j
+    int id = -1, top = 0;
     for (int j = 0; j < k; ++j) {
-        uint64_t best = 0;
+        uint32_t lb = 0;
 #pragma unroll
-        for (int c = 0; c < NPL; ++c) best = key[c] > best ? key[c] : best;
-        best = route_warp_max(best);
+        for (int c = 0; c < NPL; ++c) lb = max(lb, key[c]);
+        const uint32_t best = __reduce_max_sync(0xffffffffu, lb);
+        uint32_t mine = 0xffffffffu;
+#pragma unroll
+        for (int c = NPL - 1; c >= 0; --c)
+            if (key[c] == best) mine = (uint32_t)(c * 32 + lane);  // ends at the lane's lowest id
+        const int pick = (int)__reduce_min_sync(0xffffffffu, mine);
 #pragma unroll
         for (int c = 0; c < NPL; ++c)
-            if (key[c] == best) key[c] = 0;  // remove the pick (keys are unique)
-        if (lane == j) mine = best;
+            if (c * 32 + lane == pick) key[c] = 0;
+        if (lane == j) id = pick;
+        if (j == 0) top = pick;
     }
-    const uint64_t top = __shfl_sync(0xffffffffu, mine, 0);
-    const int id = (int)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
     const float v = (lane < k) ? __ldg(row + id) : 0.f;
-    const float m = __ldg(row + (int)(0xffffffffu - (uint32_t)(top & 0xffffffffu)));
+    const float m = __ldg(row + top);
     const float ex = (lane < k) ? expf(v - m) : 0.f;
     // sum over the k picks in slot order, the same sequential order in every lane
     float sum = 0.f;
