@@ -128,8 +128,8 @@ def test_stalled_grid_barrier_reports_timeout_and_context_survives(moe):
 
 @pytest.mark.parametrize("name", ["prefill_ep_rank", "skewed"])
 def test_layer_split_path_equals_split_entries(moe, name):
-    # moe_layer above the fused threshold gathers the token rows straight from x in
-    # its gate/up GEMM; composing the public entries goes through x_perm instead
+    # moe_layer above the fused threshold runs the router with the dispatch histograms
+    # and both GEMMs in one launch; composing the public entries must give the same bytes
     cfg, inp = inputs(name)
     dims = moe.Dims.of(cfg)
     assert dims.T * dims.k > moe.FUSED_MAX_PAIRS
