@@ -106,10 +106,10 @@ __device__ bool grid_sync(const FusedArgs& a, unsigned target, FusedSmem& fs) {
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    moe_layer_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
-                           const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
-                           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmXs,
-                           const __grid_constant__ CUtensorMap tmHs, const FusedArgs a) {
+    moe_layer_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ WMaps wmGU,
+                           const __grid_constant__ CUtensorMap tmH, const __grid_constant__ WMaps wmD,
+                           const __grid_constant__ CUtensorMap tmXs, const __grid_constant__ CUtensorMap tmHs,
+                           const FusedArgs a) {
     // tmXs / tmHs: x_perm / h with SMALL_ROWS-row boxes, for m-tiles with that few rows
     // (decode has ~16 tokens per expert: 4x less token-tile traffic than 128-row boxes)
     extern __shared__ uint8_t smem_raw[];
@@ -124,12 +124,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     init(c);
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmX);
-        tma_prefetch_desc(&tmG);
-        tma_prefetch_desc(&tmU);
         tma_prefetch_desc(&tmH);
-        tma_prefetch_desc(&tmD);
         tma_prefetch_desc(&tmXs);
         tma_prefetch_desc(&tmHs);
+        for (int i = 0; i < 3; ++i) {
+            tma_prefetch_desc(&wmGU.b0[i]);
+            tma_prefetch_desc(&wmGU.b1[i]);
+            tma_prefetch_desc(&wmD.b0[i]);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -238,9 +240,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) {
         const Args ga{a.h, a.status, n, a.H / BK, (a.I + a.bn / 2 - 1) / (a.bn / 2), a.I, a.I, a.bn / 2, 0, a.bn,
                       SMALL_ROWS};
-        build_tile_table(c, n, ga.ntiles_n);
+        build_tile_table(c, n, ga.ntiles_n, ga.bn);
         __syncthreads();
-        run_phase<MODE_GATEUP>(c, ring, p, &tmX, &tmG, &tmU, ga, &tmXs);
+        run_phase<MODE_GATEUP>(c, ring, p, &tmX, &wmGU, ga, &tmXs);
         ok = grid_sync(a, 3u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }
 
@@ -248,9 +250,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) {
         // no weight prefetch here: measured slower in this launch
         const Args da{a.y_perm, a.status, n, a.I / BK, (a.H + a.bn - 1) / a.bn, a.H, a.H, a.bn, 0, a.bn, SMALL_ROWS};
-        build_tile_table(c, n, da.ntiles_n);
+        build_tile_table(c, n, da.ntiles_n, da.bn);
         __syncthreads();
-        run_phase<MODE_DOWN>(c, ring, p, &tmH, &tmD, &tmD, da, &tmHs);
+        run_phase<MODE_DOWN>(c, ring, p, &tmH, &wmD, da, &tmHs);
         ok = grid_sync(a, 4u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }
 
@@ -283,11 +285,11 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     // each tile then reloads its token tile for half the work.)
     const int grid = sm_count();
     const int bn = BN;
-    CUtensorMap mX, mG, mU, mH, mD, mXs, mHs;
+    CUtensorMap mX, mH, mXs, mHs;
+    WMaps wGU, wD;
     if (!make_tmap_bf16(&mXs, x_perm, rows, H, SMALL_ROWS) || !make_tmap_bf16(&mHs, h, rows, I, SMALL_ROWS) ||
-        !make_tmap_bf16(&mX, x_perm, rows, H, BM) || !make_tmap_bf16(&mG, w_gate, (long long)n * I, H, bn / 2) ||
-        !make_tmap_bf16(&mU, w_up, (long long)n * I, H, bn / 2) || !make_tmap_bf16(&mH, h, rows, I, BM) ||
-        !make_tmap_bf16(&mD, w_down, (long long)n * H, I, bn))
+        !make_tmap_bf16(&mX, x_perm, rows, H, BM) || !make_wmaps(&wGU, w_gate, w_up, (long long)n * I, H, bn / 2) ||
+        !make_tmap_bf16(&mH, h, rows, I, BM) || !make_wmaps(&wD, w_down, nullptr, (long long)n * H, I, bn))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
@@ -304,7 +306,7 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_layer_fused_kernel, mX, mG, mU, mH, mD, mXs, mHs, a);
+    return cudaLaunchKernelEx(&cfg, moe_layer_fused_kernel, mX, wGU, mH, wD, mXs, mHs, a);
 }
 
 }  // namespace moe

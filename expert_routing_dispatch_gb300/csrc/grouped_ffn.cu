@@ -30,8 +30,8 @@ struct FfnArgs {
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                       const __grid_constant__ CUtensorMap tmB1, const FfnArgs args) {
+    grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
+                       const FfnArgs args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t ring = ring_base(smem_raw);
     Ctl& c = ctl_of(smem_raw);
@@ -40,19 +40,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     init(c);
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB0);
-        if (MODE == MODE_GATEUP) tma_prefetch_desc(&tmB1);
+        for (int i = 0; i < 3; ++i) {
+            tma_prefetch_desc(&wm.b0[i]);
+            if (MODE == MODE_GATEUP) tma_prefetch_desc(&wm.b1[i]);
+        }
     }
     for (int i = threadIdx.x; i <= n; i += NUM_THREADS) c.row_off[i] = __ldg(args.offsets + i);
     __syncthreads();
-    build_tile_table(c, n, args.g.ntiles_n);
+    build_tile_table(c, n, args.g.ntiles_n, args.g.bn);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     Pipe p;
     pipe_reset(p);
-    run_phase<MODE>(c, ring, p, &tmA, &tmB0, &tmB1, args.g);
+    run_phase<MODE>(c, ring, p, &tmA, &wm, args.g);
 
     __syncthreads();
     teardown(c, p, args.g.status);
@@ -93,6 +95,16 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, int cols, i
     return r == CUDA_SUCCESS;
 }
 
+// Weight maps of a GEMM whose tiles cover `rows` weight rows of each map: boxes of
+// rows, rows / 2 and rows / 4 (the split pieces of the last round)
+bool make_wmaps(WMaps* m, const void* w0, const void* w1, long long total_rows, int cols, int rows) {
+    for (int i = 0; i < 3; ++i) {
+        if (!make_tmap_bf16(&m->b0[i], w0, total_rows, cols, rows >> i)) return false;
+        if (!make_tmap_bf16(&m->b1[i], w1 ? w1 : w0, total_rows, cols, rows >> i)) return false;
+    }
+    return true;
+}
+
 namespace {
 
 template <int MODE>
@@ -111,12 +123,12 @@ cudaError_t launch_gate_up(const uint16_t* x_perm, const int32_t* offsets, const
                            cudaStream_t s) {
     cudaError_t e;
     if ((e = set_smem_attr<MODE_GATEUP>()) != cudaSuccess) return e;
-    CUtensorMap mA, mG, mU;
-    if (!make_tmap_bf16(&mA, x_perm, rows, H, BM) || !make_tmap_bf16(&mG, w_gate, (long long)n * I, H, BN / 2) ||
-        !make_tmap_bf16(&mU, w_up, (long long)n * I, H, BN / 2))
+    CUtensorMap mA;
+    WMaps wm;
+    if (!make_tmap_bf16(&mA, x_perm, rows, H, BM) || !make_wmaps(&wm, w_gate, w_up, (long long)n * I, H, BN / 2))
         return cudaErrorInvalidValue;
     FfnArgs a{offsets, {h, status, n, H / BK, (I + BN / 2 - 1) / (BN / 2), I, I, BN / 2, kPrefetchGateUp, BN, 0}};
-    grouped_ffn_kernel<MODE_GATEUP><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mA, mG, mU, a);
+    grouped_ffn_kernel<MODE_GATEUP><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mA, wm, a);
     return cudaGetLastError();
 }
 
@@ -124,11 +136,12 @@ cudaError_t launch_down(const uint16_t* h, const int32_t* offsets, const uint16_
                         long long rows, int H, int I, int n, int32_t* status, cudaStream_t s) {
     cudaError_t e;
     if ((e = set_smem_attr<MODE_DOWN>()) != cudaSuccess) return e;
-    CUtensorMap mH, mD;
-    if (!make_tmap_bf16(&mH, h, rows, I, BM) || !make_tmap_bf16(&mD, w_down, (long long)n * H, I, BN))
+    CUtensorMap mH;
+    WMaps wm;
+    if (!make_tmap_bf16(&mH, h, rows, I, BM) || !make_wmaps(&wm, w_down, nullptr, (long long)n * H, I, BN))
         return cudaErrorInvalidValue;
     FfnArgs a{offsets, {y_perm, status, n, I / BK, (H + BN - 1) / BN, H, H, BN, kPrefetchDown, BN, 0}};
-    grouped_ffn_kernel<MODE_DOWN><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mH, mD, mD, a);
+    grouped_ffn_kernel<MODE_DOWN><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mH, wm, a);
     return cudaGetLastError();
 }
 

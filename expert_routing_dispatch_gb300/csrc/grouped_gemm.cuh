@@ -13,6 +13,9 @@
 // Tiles are (expert, m-tile of 128 rows, n-tile); the tile table is built on
 // the device from the row offsets.  Within an expert the m-tiles of one n-tile
 // are consecutive, so CTAs running side by side share a weight tile through L2.
+// When the last round of tiles would leave most CTAs idle (r tiles, 2r or 4r <=
+// CTAs), each of those r tiles is split along N into 2 or 4 pieces (narrower
+// MMA N, weight boxes and epilogue), which spreads the last round over more SMs.
 //
 // CTA = 6 warps: warp 0 issues TMA loads (128-byte swizzle) into a 4-stage
 // shared-memory ring; warp 1 owns 512 TMEM columns (two 256-column fp32
@@ -83,6 +86,9 @@ struct Ctl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    int tail_first;                 // first tile of the last round
+    int tail_shift;                 // its tiles are split into 1 << tail_shift pieces along N
+    int tile_total;                 // tiles plus extra pieces: the length of the tile stream
     int tile_start[MAX_LOCAL + 1];  // exclusive prefix of tiles per expert
     int row_off[MAX_LOCAL + 1];     // grouped-row offsets of the local experts
 };
@@ -112,6 +118,14 @@ struct Pipe {
 
 struct TileCoord {
     int e, mt, nt, cnt;
+    int shift, piece;  // piece `piece` of 1 << shift along N (0, 0 for a whole tile)
+};
+
+// Weight maps of one GEMM: box heights of a whole tile and of its half and quarter
+// pieces.  b0 = W_gate (gate/up) or W_down, b1 = W_up (gate/up only).
+struct WMaps {
+    CUtensorMap b0[3];
+    CUtensorMap b1[3];
 };
 
 // Shared memory: 1024-aligned stage ring followed by the control block.
@@ -150,8 +164,9 @@ __device__ __forceinline__ void pipe_reset(Pipe& p) {
     for (int s = 0; s < STAGES; ++s) p.issued[s] = 0;
 }
 
-// warp 0: tile_start from row_off (must be in shared memory already).
-__device__ __forceinline__ void build_tile_table(Ctl& c, int n, int ntiles_n) {
+// warp 0: tile_start from row_off (must be in shared memory already), then the
+// split of the last round (pieces at least 64 weight rows wide).
+__device__ __forceinline__ void build_tile_table(Ctl& c, int n, int ntiles_n, int bn) {
     if ((threadIdx.x >> 5) != 0) return;
     const int lane = threadIdx.x & 31;
     int carry = 0;
@@ -167,17 +182,37 @@ __device__ __forceinline__ void build_tile_table(Ctl& c, int n, int ntiles_n) {
         if (e < n) c.tile_start[e + 1] = carry + v;
         carry += __shfl_sync(0xffffffffu, v, 31);
     }
-    if (lane == 0) c.tile_start[0] = 0;
+    if (lane == 0) {
+        c.tile_start[0] = 0;
+        const int total = carry, G = (int)gridDim.x, r = total % G;
+        int sh = 0;
+        if (r > 0 && 4 * r <= G && (bn >> 2) >= 64)
+            sh = 2;
+        else if (r > 0 && 2 * r <= G && (bn >> 1) >= 64)
+            sh = 1;
+        c.tail_first = total - r;
+        c.tail_shift = sh;
+        c.tile_total = total - r + (r << sh);
+    }
 }
 
 __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_hint, TileCoord& tc) {
-    if (tile >= c.tile_start[n]) return false;
+    if (tile >= c.tile_total) return false;
+    int f = tile;  // whole tile of this stream position
+    tc.shift = 0;
+    tc.piece = 0;
+    if (tile >= c.tail_first) {
+        const int h = tile - c.tail_first;
+        tc.shift = c.tail_shift;
+        f = c.tail_first + (h >> tc.shift);
+        tc.piece = h & ((1 << tc.shift) - 1);
+    }
     int e = e_hint;
-    while (c.tile_start[e + 1] <= tile) ++e;  // tiles increase monotonically per CTA
+    while (c.tile_start[e + 1] <= f) ++e;  // tiles increase monotonically per CTA
     e_hint = e;
     const int cnt = c.row_off[e + 1] - c.row_off[e];
     const int mtiles = (cnt + BM - 1) / BM;
-    const int local = tile - c.tile_start[e];
+    const int local = f - c.tile_start[e];
     tc.e = e;
     tc.nt = local / mtiles;
     tc.mt = local - tc.nt * mtiles;
@@ -190,9 +225,8 @@ __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_
 //   m-tile with at most a_small valid rows loads only those rows; the MMA still
 //   reads 128 rows, and the stale ones only feed output rows that are not stored.
 template <int MODE>
-__device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const CUtensorMap* tmA,
-                                          const CUtensorMap* tmB0, const CUtensorMap* tmB1, const Args& args,
-                                          const CUtensorMap* tmA_small = nullptr) {
+__device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const CUtensorMap* tmA, const WMaps* wm,
+                                          const Args& args, const CUtensorMap* tmA_small = nullptr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = args.n;
     volatile int* abort_flag = &c.abort_flag;
@@ -224,10 +258,14 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             bool ok = !*abort_flag;
             for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
                 const int a_row = c.row_off[tc.e] + tc.mt * BM;
-                const int b_row = tc.e * args.b_rows + tc.nt * args.n_step;
+                const int piece_rows = args.n_step >> tc.shift;  // weight rows of one map's box
+                const int b_row = tc.e * args.b_rows + tc.nt * args.n_step + tc.piece * piece_rows;
+                const int bn_t = args.bn >> tc.shift;
+                const CUtensorMap* tmB0 = &wm->b0[tc.shift];
+                const CUtensorMap* tmB1 = &wm->b1[tc.shift];
                 const bool a_small = tmA_small != nullptr && tc.cnt - tc.mt * BM <= args.a_small;
                 const CUtensorMap* tma_a = a_small ? tmA_small : tmA;
-                const uint32_t stage_tx = (uint32_t)((a_small ? args.a_small : BM) * BK * 2 + args.bn * BK * 2);
+                const uint32_t stage_tx = (uint32_t)((a_small ? args.a_small : BM) * BK * 2 + bn_t * BK * 2);
                 for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                     const int s = p.g % STAGES, r = p.g / STAGES;
                     if (!MOE_PROF_WAIT(w_empty, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
@@ -238,7 +276,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     // The first m-tile of each weight tile pulls the weight boxes PF k-blocks
                     // ahead into L2 (only boxes wholly inside the tensor).
                     const int PF = args.prefetch;
-                    if (PF > 0 && tc.mt == 0 && kb + PF < args.kblocks &&
+                    if (PF > 0 && tc.shift == 0 && tc.mt == 0 && kb + PF < args.kblocks &&
                         b_row + (MODE == MODE_GATEUP ? args.bn / 2 : args.bn) <= n * args.b_rows) {
                         tma_prefetch_l2_2d(tmB0, (kb + PF) * BK, b_row);
                         if (MODE == MODE_GATEUP) tma_prefetch_l2_2d(tmB1, (kb + PF) * BK, b_row);
@@ -247,9 +285,9 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     mbar_arrive_expect_tx(fb, stage_tx);
                     p.issued[s] = r + 1;
                     tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
-                    if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn/2 each
+                    if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn_t/2 each
                         tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
-                        tma_load_2d(b_addr(s) + (uint32_t)(args.bn / 2) * BK * 2, tmB1, kb * BK, b_row, fb, pol_b);
+                        tma_load_2d(b_addr(s) + (uint32_t)(bn_t / 2) * BK * 2, tmB1, kb * BK, b_row, fb, pol_b);
                     } else {
                         tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
                     }
@@ -279,7 +317,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * BN);
-                const uint32_t idesc = idesc_bf16_f32(BM, args.bn);
+                const uint32_t idesc = idesc_bf16_f32(BM, args.bn >> tc.shift);
                 for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                     const int s = p.g % STAGES, r = p.g / STAGES;
                     if (!MOE_PROF_WAIT(w_full, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status,
@@ -323,18 +361,19 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             const int row0_in_e = tc.mt * BM + q * 32;  // first row of this warp's block
             const long long grow0 = (long long)c.row_off[tc.e] + row0_in_e;
             const uint32_t taddr = c.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            const int col0 = tc.nt * args.n_step;
+            const int bn_t = args.bn >> tc.shift;
+            const int col0 = tc.nt * args.n_step + tc.piece * (args.n_step >> tc.shift);
             uint4* st = c.stage[q];
             if (MODE == MODE_GATEUP) {
                 // 32 h columns per chunk: 64 B per row, 4 slots; slot = piece ^ ((row >> 1) & 3)
                 uint16_t* out = static_cast<uint16_t*>(args.out);
 #pragma unroll 1
-                for (int cc = 0; cc < args.bn / 2; cc += 32) {
+                for (int cc = 0; cc < bn_t / 2; cc += 32) {
                     uint32_t g0[16], g1[16], u0[16], u1[16];
                     tmem_ld16(taddr + cc, g0);
                     tmem_ld16(taddr + cc + 16, g1);
-                    tmem_ld16(taddr + args.bn / 2 + cc, u0);
-                    tmem_ld16(taddr + args.bn / 2 + cc + 16, u1);
+                    tmem_ld16(taddr + bn_t / 2 + cc, u0);
+                    tmem_ld16(taddr + bn_t / 2 + cc + 16, u1);
                     tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
@@ -366,7 +405,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                 // 32 fp32 columns per chunk: 128 B per row, 8 slots; slot = piece ^ (row & 7)
                 float* out = static_cast<float*>(args.out);
 #pragma unroll 1
-                for (int cc = 0; cc < args.bn; cc += 32) {
+                for (int cc = 0; cc < bn_t; cc += 32) {
                     uint32_t v0[16], v1[16];
                     tmem_ld16(taddr + cc, v0);
                     tmem_ld16(taddr + cc + 16, v1);

@@ -53,6 +53,13 @@ cudaError_t launch_down(const uint16_t* h, const int32_t* offsets, const uint16_
 // (128 B, 128-byte swizzle) x box_rows rows
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, long long rows, int cols, int box_rows);
 
+// Weight maps of one grouped GEMM (grouped_gemm.cuh): boxes of `rows`, rows / 2 and
+// rows / 4 weight rows over W0 (and W1, or W0 again when w1 is NULL)
+namespace gemm {
+struct WMaps;
+}
+bool make_wmaps(gemm::WMaps* m, const void* w0, const void* w1, long long total_rows, int cols, int rows);
+
 // decode_fused.cu: the whole layer in one persistent cooperative launch
 cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uint16_t* w_gate, const uint16_t* w_up,
                                const uint16_t* w_down, float* out, int32_t* topk_idx, float* topk_w,

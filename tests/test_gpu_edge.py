@@ -91,6 +91,24 @@ def test_layer_small_shapes(moe, dims):
     check_layer(moe, moe.Dims(*dims), inp)
 
 
+# The same kinds of edges above the fused threshold (T*k > 8192 pairs), so they run
+# the split kernels: ragged H / I tails (a partial last weight tile in both GEMMs),
+# E not a multiple of 32 with a partial range, a single local expert with an m-tile
+# tail, and k = E.  The oracle checks a sample of tokens (all of them when small).
+@pytest.mark.parametrize("dims", [
+    (4200, 320, 192, 6, 2, 0, 6),     # ragged H (256+64) and I (128+64) tails
+    (2000, 192, 320, 40, 5, 7, 33),   # E not a multiple of 32, partial range, I = 2.5 gate/up tiles
+    (9000, 256, 128, 3, 1, 1, 2),     # single local expert, 9000 rows = 70 m-tiles + 40
+    (1100, 448, 704, 8, 8, 2, 5),     # k = E, partial range, H = 1.75 down tiles, I = 5.5 gate/up tiles
+])
+def test_layer_small_shapes_split_path(moe, dims):
+    T, k = dims[0], dims[4]
+    assert T * k > moe.FUSED_MAX_PAIRS
+    inp = small_inputs(*dims)
+    toks = None if T <= 2000 else np.unique(np.r_[np.arange(0, T, 7), T - 1])
+    check_layer(moe, moe.Dims(*dims), inp, tokens=toks)
+
+
 def test_empty_local_range(moe):
     # all-equal logits: every token picks experts 0..3, so [8, 16) receives nothing (R = 0)
     T, H, I, E, k, e0, e1 = dims = (64, 256, 128, 16, 4, 8, 16)
