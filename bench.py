@@ -2,12 +2,14 @@
 """Benchmark of the local MoE layer of one expert-parallel rank on GB300.
 
 One step = one pass of the whole hot path over one batch of seeded synthetic
-input: route -> dispatch -> gate/up GEMM + SwiGLU -> down GEMM -> combine.  For
-prefill-sized workloads each step is launched through the C ABI on one stream
-with CUDA events between the calls (the same kernels moe_layer launches); for
-decode-sized ones (T*k <= MOE_FUSED_MAX_PAIRS) it is moe_layer's single fused
-launch.  Inputs are resident in HBM; L2 is flushed (256 MiB write) between
-timed steps, outside the timed region.
+input: route -> dispatch -> gate/up GEMM + SwiGLU -> down GEMM -> combine, as
+one moe_layer call through the C ABI (its split kernels for prefill-sized
+workloads, its single fused launch for decode-sized ones, T*k <=
+MOE_FUSED_MAX_PAIRS).  For the split path a second loop calls the step's
+entries one by one (moe_route, moe_dispatch, moe_expert_gate_up,
+moe_expert_down, moe_combine) with CUDA events between them, for the per-kernel
+breakdown and the gate/up GEMM's roofline.  Inputs are resident in HBM; L2 is
+flushed (256 MiB write) between timed steps, outside the timed region.
 
 Prints one JSON line.  `value` is routed tokens/s (T / step time, summed over
 replicas for N > 1: every rank runs its own replica, no collective on the data
@@ -284,21 +286,22 @@ def run_ours(args):
 
     lws = moe.alloc_workspace(moe.moe_workspace_size(dims), dev)
     fused = P <= moe.FUSED_MAX_PAIRS
-    if fused:
-        # decode-sized: moe_layer is one persistent launch (route..combine fused)
-        names = ["layer_fused"]
-        launches_per_step = 1
+    # the timed step: one moe_layer call (decode-sized: one persistent launch; else
+    # route + dispatch place/gather + gate/up + down + combine)
+    names = ["layer_fused" if fused else "layer"]
+    launches_per_step = 1 if fused else 6
 
-        def step(evs):
-            evs[0].record(stream)
-            moe.moe_layer(dims, x, lg, wg, wu, wd, out, lws, topk_idx=topk_idx, topk_w=topk_w, status=status,
-                          stream=sh)
-            evs[1].record(stream)
-    else:
-        names = ["route", "dispatch", "gate_up", "down", "combine"]
-        launches_per_step = 1 + 4 + 1 + 1 + 1
+    def step(evs):
+        evs[0].record(stream)
+        moe.moe_layer(dims, x, lg, wg, wu, wd, out, lws, topk_idx=topk_idx, topk_w=topk_w, status=status,
+                      stream=sh)
+        evs[1].record(stream)
 
-        def step(evs):
+    if not fused:
+        # breakdown loop (not the headline): the same work as separate entry calls
+        bnames = ["route", "dispatch", "gate_up", "down", "combine"]
+
+        def bstep(evs):
             evs[0].record(stream)
             moe.moe_route(dims, lg, topk_idx, topk_w, status, stream=sh)
             evs[1].record(stream)
@@ -311,7 +314,7 @@ def run_ours(args):
             moe.moe_combine(dims, y_perm, pair_row, topk_w, out, stream=sh)
             evs[5].record(stream)
 
-    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+    mk = lambda k=len(names): [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
     for _ in range(args.warmup):
         flush.zero_()
         step(mk())
@@ -334,14 +337,23 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
-    per_kernel = {nm: [] for nm in names}
-    step_ms = []
-    for evs in all_evs:
-        step_ms.append(evs[0].elapsed_time(evs[-1]))
-        for i, nm in enumerate(names):
-            per_kernel[nm].append(evs[i].elapsed_time(evs[i + 1]))
+    step_ms = [evs[0].elapsed_time(evs[-1]) for evs in all_evs]
     t_step = sum(step_ms) / len(step_ms)
-    kern_ms = {nm: sum(v) / len(v) for nm, v in per_kernel.items()}
+    kern_ms = {names[0]: t_step}
+    if not fused:
+        # per-kernel breakdown from the entry-by-entry loop (same warm-up, flush and step count)
+        b_evs = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            evs = mk(len(bnames))
+            bstep(evs)
+            if i >= args.warmup:
+                b_evs.append(evs)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
+        for i, nm in enumerate(bnames):
+            kern_ms[nm] = sum(e[i].elapsed_time(e[i + 1]) for e in b_evs) / len(b_evs)
+        kern_ms["entries_total"] = sum(e[0].elapsed_time(e[-1]) for e in b_evs) / len(b_evs)
     # routed rows and active local experts, counted from this run's routing
     ti = topk_idx.flatten()
     loc = ti[(ti >= e0) & (ti < e1)]
