@@ -48,6 +48,12 @@ def _bind(lib):
     lib.oracle_combine_tokens.restype = None
     lib.oracle_moe_layer_tokens.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp]
     lib.oracle_moe_layer_tokens.restype = i32
+    lib.oracle_mxfp8_quantize.argtypes = [i64, i32, vp, vp, vp]
+    lib.oracle_mxfp8_quantize.restype = i32
+    lib.oracle_mxfp8_dequantize.argtypes = [i64, i32, vp, vp, vp]
+    lib.oracle_mxfp8_dequantize.restype = None
+    lib.oracle_expert_ffn_mxfp8_rowlist.argtypes = [i32, i32, i32] + [vp] * 9 + [vp, i64] + [vp] * 6
+    lib.oracle_expert_ffn_mxfp8_rowlist.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     return lib
@@ -151,3 +157,47 @@ def moe_layer_tokens(logits, x, w_gate, w_up, w_down, k, e0, e1, tokens=None):
     st = _load().oracle_moe_layer_tokens(H, I, E, k, e0, e1, _p(lg), _p(xx), _p(wg), _p(wu), _p(wd),
                                          _p(toks), toks.size, _p(out))
     return int(st), out
+
+
+# ---------------------------------------------------------------- MXFP8
+def mxfp8_quantize(a):
+    """MXFP8 (E4M3 elements, UE8M0 scales, blocks of 32 along the last axis) of a
+    bf16 bit-pattern matrix [rows, K] -> (q uint8 [rows, K], s uint8 [rows, K/32])."""
+    src = _c(a, np.uint16)
+    rows, K = src.shape
+    q = np.empty((rows, K), np.uint8)
+    s = np.empty((rows, K // 32), np.uint8)
+    if _load().oracle_mxfp8_quantize(rows, K, _p(src), _p(q), _p(s)) != 0:
+        raise ValueError("oracle_mxfp8_quantize: K must be a multiple of 32")
+    return q, s
+
+
+def mxfp8_dequantize(q, s):
+    """float64 values of an MXFP8 matrix."""
+    qq, ss = _c(q, np.uint8), _c(s, np.uint8)
+    rows, K = qq.shape
+    out = np.empty((rows, K), np.float64)
+    _load().oracle_mxfp8_dequantize(rows, K, _p(qq), _p(ss), _p(out))
+    return out
+
+
+def expert_ffn_mxfp8_rowlist(xq, xs, offsets, wg, wu, wd, rows, h_in=None, want_h=False):
+    """MXFP8 expert FFN of the listed grouped rows.  wg, wu, wd are (q, s) pairs with
+    the shapes of the bf16 weights ([n, I, H], [n, I, H], [n, H, I]) and of their
+    scales.  h_in: optional (hq, hs) [len(rows), I] / [len(rows), I/32] used for the
+    down GEMM instead of the oracle's own quantised h.  Returns y float64
+    [len(rows), H], and with want_h also (h fp64, hq, hs) of the oracle's h."""
+    xq_, xs_ = _c(xq, np.uint8), _c(xs, np.uint8)
+    H = xq_.shape[1]
+    n, I, _ = wg[0].shape
+    off, rr = _c(offsets, np.int32), _c(rows, np.int64)
+    w = [_c(a, np.uint8) for pair in (wg, wu, wd) for a in pair]
+    y = np.zeros((rr.size, H), np.float64)
+    h = np.zeros((rr.size, I), np.float64) if want_h else None
+    hq = np.zeros((rr.size, I), np.uint8) if want_h else None
+    hs = np.zeros((rr.size, I // 32), np.uint8) if want_h else None
+    hin = [None, None] if h_in is None else [_c(h_in[0], np.uint8), _c(h_in[1], np.uint8)]
+    p = lambda a: None if a is None else _p(a)
+    _load().oracle_expert_ffn_mxfp8_rowlist(H, I, n, _p(xq_), _p(xs_), _p(off), *[_p(a) for a in w], _p(rr),
+                                            rr.size, p(hin[0]), p(hin[1]), p(h), p(hq), p(hs), _p(y))
+    return (y, h, hq, hs) if want_h else y

@@ -255,6 +255,175 @@ int oracle_moe_layer_tokens(int H, int I, int E, int k, int e0, int e1, const fl
     return status;
 }
 
+/*
+ * MXFP8: "Hosting Qwen on Blackwell", section "MoE GEMM": the deployed expert
+ * GEMMs use MXFP8.  The pages give no format details; the plain reading is the
+ * OCP Microscaling Formats (MX) v1.0 definition of MXFP8:
+ *   - blocks of 32 consecutive elements along K share one UE8M0 scale
+ *     X = 2^(code - 127) (code 255 = NaN is never produced);
+ *   - X = 2^(floor(log2(amax)) - 8), 8 being the largest exponent of an E4M3
+ *     normal number (448 = 1.75 * 2^8), with amax the block's largest |v|; a
+ *     block of zeros gets code 0; the code is clamped to [0, 254];
+ *   - each element is v / X rounded to the nearest E4M3 value (ties to an even
+ *     mantissa), saturating at +-448 (E4M3 has no infinities; 0x7f / 0xff are
+ *     NaN); a negative value keeps its sign bit even when it rounds to zero.
+ * E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 holds the
+ * subnormals m * 2^-9.
+ */
+static double e4m3_decode(uint8_t b) {
+    const int e = (b >> 3) & 15, m = b & 7;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return (b & 0x80) ? -v : v;
+}
+
+/* nearest E4M3 code of v (|v| is the element divided by its block scale) */
+static uint8_t e4m3_encode(double v) {
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7e; /* saturate (also the rounding of 448..464) */
+    int e;
+    double q;                           /* quantum of a's binade */
+    if (a < ldexp(1.0, -6)) {
+        e = -6;                         /* subnormal range: steps of 2^-9 */
+        q = ldexp(1.0, -9);
+    } else {
+        e = (int)floor(log2(a));
+        if (ldexp(1.0, e) > a) --e;     /* guard log2 rounding */
+        if (ldexp(1.0, e + 1) <= a) ++e;
+        q = ldexp(1.0, e - 3);
+    }
+    double m = nearbyint(a / q);        /* ties to even (default rounding mode) */
+    double val = m * q;                 /* exact, at most 448 since a < 448 */
+    if (val == 0.0) return sign;
+    /* re-derive the code of the exactly representable value */
+    if (val < ldexp(1.0, -6)) return sign | (uint8_t)(val / ldexp(1.0, -9));
+    int ve = (int)floor(log2(val));
+    if (ldexp(1.0, ve) > val) --ve;
+    if (ldexp(1.0, ve + 1) <= val) ++ve;
+    const int mant = (int)(val / ldexp(1.0, ve - 3)) - 8;
+    return sign | (uint8_t)(((ve + 7) << 3) | mant);
+}
+
+/* scale code of a block whose largest magnitude is amax */
+static uint8_t mx_scale_code(double amax) {
+    if (amax == 0.0) return 0;
+    int p = (int)floor(log2(amax));
+    if (ldexp(1.0, p) > amax) --p;
+    if (ldexp(1.0, p + 1) <= amax) ++p;
+    int c = p - 8 + 127;
+    return (uint8_t)(c < 0 ? 0 : c > 254 ? 254 : c);
+}
+
+/* quantise len values (len <= 32) of one block */
+static void mx_quantize_block(const double* v, int len, uint8_t* q, uint8_t* s) {
+    double amax = 0.0;
+    for (int i = 0; i < len; ++i) amax = fmax(amax, fabs(v[i]));
+    *s = mx_scale_code(amax);
+    const double x = ldexp(1.0, (int)*s - 127);
+    for (int i = 0; i < len; ++i) q[i] = e4m3_encode(v[i] / x);
+}
+
+/*
+ * MXFP8 quantisation of a bf16 matrix [rows, K] along K: q uint8 [rows, K] (E4M3
+ * codes), s uint8 [rows, K / 32] (UE8M0 codes).  K must be a multiple of 32.
+ */
+int oracle_mxfp8_quantize(int64_t rows, int K, const uint16_t* src, uint8_t* q, uint8_t* s) {
+    if (rows < 0 || K <= 0 || K % 32) return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double v[32];
+        for (int b = 0; b < K / 32; ++b) {
+            for (int i = 0; i < 32; ++i) v[i] = bf16_widen(src[r * K + b * 32 + i]);
+            mx_quantize_block(v, 32, q + r * K + b * 32, s + r * (K / 32) + b);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* one row of K elements: out[k] = E4M3(q[k]) * 2^(s[k / 32] - 127) */
+static void mx_dequantize_row(int K, const uint8_t* q, const uint8_t* s, double* out) {
+    for (int k = 0; k < K; ++k) out[k] = e4m3_decode(q[k]) * ldexp(1.0, (int)s[k / 32] - 127);
+}
+
+/* out[r, k] = E4M3(q[r, k]) * 2^(s[r, k / 32] - 127), in fp64 */
+void oracle_mxfp8_dequantize(int64_t rows, int K, const uint8_t* q, const uint8_t* s, double* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) mx_dequantize_row(K, q + r * K, s + r * (K / 32), out + r * K);
+}
+
+/*
+ * The expert FFN with MXFP8 operands, on an explicit list of grouped rows: the
+ * gate/up GEMM on the dequantised x_perm row and weights (fp64), h = silu(g) * u
+ * (fp64), h quantised to MXFP8 along I (blocks of 32, the same rule), then the
+ * down GEMM on the dequantised h and W_down (fp64).
+ *   xq/xs: x_perm [*, H] / [*, H/32];  wgq, wuq [n, I, H] with wgs, wus [n, I, H/32];
+ *   wdq [n, H, I] with wds [n, H, I/32].
+ *   h_in_q / h_in_s (optional, [nrows, I] / [nrows, I/32]): use this quantised h
+ *   for the down GEMM instead of the oracle's own (to check a down GEMM alone).
+ *   h_out (optional, fp64 [nrows, I]): h before quantisation;
+ *   hq_out / hs_out (optional): the oracle's quantised h.
+ * y: fp64 [nrows, H].  Rows outside every expert get y = 0.
+ */
+void oracle_expert_ffn_mxfp8_rowlist(int H, int I, int n, const uint8_t* xq, const uint8_t* xs,
+                                     const int32_t* offsets, const uint8_t* wgq, const uint8_t* wgs,
+                                     const uint8_t* wuq, const uint8_t* wus, const uint8_t* wdq, const uint8_t* wds,
+                                     const int64_t* rows, int64_t nrows, const uint8_t* h_in_q,
+                                     const uint8_t* h_in_s, double* h_out, uint8_t* hq_out, uint8_t* hs_out,
+                                     double* y) {
+#pragma omp parallel
+    {
+        double* xd = (double*)malloc(sizeof(double) * (size_t)H);
+        double* w = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
+        double* h = (double*)malloc(sizeof(double) * (size_t)I);
+        double* hd = (double*)malloc(sizeof(double) * (size_t)I);
+        uint8_t* hq = (uint8_t*)malloc((size_t)I);
+        uint8_t* hs = (uint8_t*)malloc((size_t)I / 32 + 1);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t qi = 0; qi < nrows; ++qi) {
+            const int64_t r = rows[qi];
+            double* yr = y + qi * H;
+            int e = -1;
+            for (int c = 0; c < n; ++c)
+                if (r >= offsets[c] && r < offsets[c + 1]) { e = c; break; }
+            if (e < 0) {
+                for (int j = 0; j < H; ++j) yr[j] = 0.0;
+                continue;
+            }
+            mx_dequantize_row(H, xq + r * H, xs + r * (H / 32), xd);
+            for (int i = 0; i < I; ++i) {
+                const int64_t wr = (int64_t)e * I + i;
+                double g = 0.0, u = 0.0;
+                mx_dequantize_row(H, wgq + wr * H, wgs + wr * (H / 32), w);
+                for (int j = 0; j < H; ++j) g += w[j] * xd[j];
+                mx_dequantize_row(H, wuq + wr * H, wus + wr * (H / 32), w);
+                for (int j = 0; j < H; ++j) u += w[j] * xd[j];
+                h[i] = g / (1.0 + exp(-g)) * u;
+            }
+            for (int b = 0; b < I / 32; ++b) mx_quantize_block(h + b * 32, 32, hq + b * 32, hs + b);
+            if (h_out) memcpy(h_out + qi * I, h, sizeof(double) * (size_t)I);
+            if (hq_out) memcpy(hq_out + qi * I, hq, (size_t)I);
+            if (hs_out) memcpy(hs_out + qi * (I / 32), hs, (size_t)I / 32);
+            if (h_in_q)
+                mx_dequantize_row(I, h_in_q + qi * I, h_in_s + qi * (I / 32), hd);
+            else
+                mx_dequantize_row(I, hq, hs, hd);
+            for (int j = 0; j < H; ++j) {
+                const int64_t wr = (int64_t)e * H + j;
+                mx_dequantize_row(I, wdq + wr * I, wds + wr * (I / 32), w);
+                double acc = 0.0;
+                for (int i = 0; i < I; ++i) acc += w[i] * hd[i];
+                yr[j] = acc;
+            }
+        }
+        free(xd);
+        free(w);
+        free(h);
+        free(hd);
+        free(hq);
+        free(hs);
+    }
+}
+
 /* number of OpenMP threads a parallel region uses (1 without OpenMP) */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

@@ -11,6 +11,7 @@ import pytest
 import oracle
 import test_oracle_dispatch as pd
 import test_oracle_ffn_combine as pf
+import test_oracle_mxfp8 as pm
 import test_oracle_route as pr
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -31,6 +32,11 @@ MUTANTS = {
                                 "o[h] += (double)y_perm[(int64_t)r * H + h];"),
     "layer_ignores_weights": ("for (int h = 0; h < H; ++h) o[h] += w[j] * y[h];",
                               "for (int h = 0; h < H; ++h) o[h] += y[h];"),
+    "mx_scale_off_by_one": ("int c = p - 8 + 127;", "int c = p - 7 + 127;"),
+    "mx_saturates_to_nan_code": ("if (a >= 448.0) return sign | 0x7e; /* saturate (also the rounding of 448..464) */",
+                                 "if (a >= 448.0) return sign | 0x7f;"),
+    "mx_round_half_away": ("double m = nearbyint(a / q);", "double m = floor(a / q + 0.5);"),
+    "mx_h_not_quantised": ("mx_dequantize_row(I, hq, hs, hd);", "memcpy(hd, h, sizeof(double) * (size_t)I);"),
 }
 
 PINS = [
@@ -45,6 +51,12 @@ PINS = [
     lambda: pf.test_dense_masked_formula(0, 6),
     lambda: pf.test_grouped_rows_match_textbook(),
     lambda: pf.test_combine_is_slot_ordered_weighted_gather(),
+    lambda: pm.test_e4m3_table_values(),
+    lambda: pm.test_nearest_code_by_exhaustive_search(),
+    lambda: pm.test_scale_code_closed_form(),
+    lambda: pm.test_ties_signed_zero_and_saturation(),
+    lambda: pm.test_mx_ffn_against_dequantised_float64(64, 32, 2),
+    lambda: pm.test_mx_ffn_near_bf16_oracle_when_operands_are_exact(),
 ]
 
 
