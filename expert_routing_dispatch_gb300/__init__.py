@@ -14,6 +14,8 @@ __all__ = [
     "MoeError", "Dims", "lib", "build", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine",
     "moe_layer", "moe_combine_accumulate", "moe_expert_gate_up", "moe_expert_down", "moe_workspace_size", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
     "moe_status_string", "alloc_workspace", "EXPORTED", "moe_testing_layer_stalled_barrier", "FUSED_MAX_PAIRS",
+    "moe_quantize_mxfp8", "moe_expert_ffn_mxfp8_workspace_size", "moe_expert_ffn_mxfp8", "moe_layer_mxfp8_workspace_size",
+    "moe_layer_mxfp8",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -23,7 +25,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmoe.so")
 EXPORTED = ("moe_status_string", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
             "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_expert_gate_up",
             "moe_expert_down", "moe_combine", "moe_combine_accumulate", "moe_layer",
-            "moe_testing_layer_stalled_barrier")
+            "moe_testing_layer_stalled_barrier", "moe_quantize_mxfp8", "moe_expert_ffn_mxfp8_workspace_size",
+            "moe_expert_ffn_mxfp8", "moe_layer_mxfp8_workspace_size", "moe_layer_mxfp8")
 
 FUSED_MAX_PAIRS = 8192  # MOE_FUSED_MAX_PAIRS in include/moe.h
 
@@ -71,7 +74,8 @@ def lib():
         pd = ctypes.POINTER(Dims)
         L.moe_status_string.argtypes = [i32]
         L.moe_status_string.restype = ctypes.c_char_p
-        for f in (L.moe_workspace_size, L.moe_dispatch_workspace_size, L.moe_expert_ffn_workspace_size):
+        for f in (L.moe_workspace_size, L.moe_dispatch_workspace_size, L.moe_expert_ffn_workspace_size,
+                  L.moe_expert_ffn_mxfp8_workspace_size, L.moe_layer_mxfp8_workspace_size):
             f.argtypes = [pd]
             f.restype = sz
         L.moe_route.argtypes = [pd, vp, vp, vp, vp, vp]
@@ -84,8 +88,12 @@ def lib():
         L.moe_combine_accumulate.argtypes = [pd, vp, vp, vp, vp, vp]
         L.moe_layer.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         L.moe_testing_layer_stalled_barrier.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+        L.moe_quantize_mxfp8.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, vp, vp, vp]
+        L.moe_expert_ffn_mxfp8.argtypes = [pd] + [vp] * 11 + [sz, vp, vp]
+        L.moe_layer_mxfp8.argtypes = [pd] + [vp] * 12 + [sz, vp, vp]
         for f in (L.moe_route, L.moe_dispatch, L.moe_dispatch_noalloc, L.moe_expert_ffn, L.moe_expert_gate_up, L.moe_expert_down,
-                  L.moe_combine, L.moe_combine_accumulate, L.moe_layer, L.moe_testing_layer_stalled_barrier):
+                  L.moe_combine, L.moe_combine_accumulate, L.moe_layer, L.moe_testing_layer_stalled_barrier,
+                  L.moe_quantize_mxfp8, L.moe_expert_ffn_mxfp8, L.moe_layer_mxfp8):
             f.restype = i32
         _lib = L
     return _lib
@@ -216,3 +224,40 @@ def moe_testing_layer_stalled_barrier(dims, x, logits, w_gate, w_up, w_down, out
     _check(lib().moe_testing_layer_stalled_barrier(ctypes.byref(d), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up),
                                                    _ptr(w_down), _ptr(out), _ptr(ws), nb, _ptr(status),
                                                    _stream(stream)), "moe_testing_layer_stalled_barrier")
+
+
+# ---------------------------------------------------------------- MXFP8
+def moe_quantize_mxfp8(src, rows, K, q, s, stream=None):
+    """q, s = MXFP8 (E4M3 codes, UE8M0 block-32 scales) of the bf16 matrix src [rows, K]."""
+    _check(lib().moe_quantize_mxfp8(_ptr(src), int(rows), int(K), _ptr(q), _ptr(s), _stream(stream)),
+           "moe_quantize_mxfp8")
+
+
+def moe_expert_ffn_mxfp8_workspace_size(dims):
+    return int(lib().moe_expert_ffn_mxfp8_workspace_size(ctypes.byref(Dims.of(dims))))
+
+
+def moe_layer_mxfp8_workspace_size(dims):
+    return int(lib().moe_layer_mxfp8_workspace_size(ctypes.byref(Dims.of(dims))))
+
+
+def moe_expert_ffn_mxfp8(dims, x_perm_q, x_perm_s, offsets, w_gate, w_up, w_down, y_perm, ws, ws_bytes=None,
+                         status=None, stream=None):
+    """w_gate, w_up, w_down: (codes, scales) pairs."""
+    d = Dims.of(dims)
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check(lib().moe_expert_ffn_mxfp8(ctypes.byref(d), _ptr(x_perm_q), _ptr(x_perm_s), _ptr(offsets),
+                                      _ptr(w_gate[0]), _ptr(w_gate[1]), _ptr(w_up[0]), _ptr(w_up[1]),
+                                      _ptr(w_down[0]), _ptr(w_down[1]), _ptr(y_perm), _ptr(ws), nb, _ptr(status),
+                                      _stream(stream)), "moe_expert_ffn_mxfp8")
+
+
+def moe_layer_mxfp8(dims, x, logits, w_gate, w_up, w_down, out, ws, ws_bytes=None, topk_idx=None, topk_w=None,
+                    status=None, stream=None):
+    """w_gate, w_up, w_down: (codes, scales) pairs from moe_quantize_mxfp8."""
+    d = Dims.of(dims)
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check(lib().moe_layer_mxfp8(ctypes.byref(d), _ptr(x), _ptr(logits), _ptr(w_gate[0]), _ptr(w_gate[1]),
+                                 _ptr(w_up[0]), _ptr(w_up[1]), _ptr(w_down[0]), _ptr(w_down[1]), _ptr(out),
+                                 _ptr(topk_idx), _ptr(topk_w), _ptr(ws), nb, _ptr(status), _stream(stream)),
+           "moe_layer_mxfp8")

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libmoe.so")
-SOURCES = ["abi.cu", "route.cu", "dispatch.cu", "combine.cu", "grouped_ffn.cu", "decode_fused.cu"]
+SOURCES = ["abi.cu", "route.cu", "dispatch.cu", "combine.cu", "grouped_ffn.cu", "decode_fused.cu", "mxfp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -90,6 +90,57 @@ LayerWs carve(const moe_dims* d, void* base) {
     return w;
 }
 
+// moe_layer_mxfp8 workspace: the routing and dispatch buffers, x and x_perm in
+// MXFP8, the MX FFN scratch (h codes and scales) and y_perm
+struct MxLayerWs {
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* row_pair;
+    int32_t* pair_row;
+    void* dispatch_ws;
+    uint8_t *xq, *xs, *xpq, *xps;
+    void* ffn_ws;
+    float* y_perm;
+    size_t dispatch_bytes, total;
+};
+
+MxLayerWs carve_mx(const moe_dims* d, void* base) {
+    MxLayerWs w{};
+    const size_t P = pairs_of(d), n = (size_t)(d->e1 - d->e0), T = (size_t)d->T, H = (size_t)d->H;
+    uint8_t* p = static_cast<uint8_t*>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* r = p ? p + off : nullptr;
+        off += align_up(bytes);
+        return r;
+    };
+    w.topk_idx = reinterpret_cast<int32_t*>(take(P * 4));
+    w.topk_w = reinterpret_cast<float*>(take(P * 4));
+    w.counts = reinterpret_cast<int32_t*>(take(n * 4));
+    w.offsets = reinterpret_cast<int32_t*>(take((n + 1) * 4));
+    w.row_pair = reinterpret_cast<int32_t*>(take(P * 4));
+    w.pair_row = reinterpret_cast<int32_t*>(take(P * 4));
+    w.dispatch_bytes = align_up(dispatch_scratch_bytes((long long)d->T, (int)n));
+    w.dispatch_ws = take(w.dispatch_bytes);
+    w.xq = take(T * H);
+    w.xs = take(T * H / 32);
+    w.xpq = take(P * H);
+    w.xps = take(P * H / 32);
+    w.ffn_ws = take(mx_ffn_scratch_bytes((long long)P, d->I));
+    w.y_perm = reinterpret_cast<float*>(take(P * H * 4));
+    w.total = off;
+    return w;
+}
+
+// MXFP8 entries: k-blocks of 128 elements along H and I
+int check_mx_dims(const moe_dims* d) {
+    const int st = check_dims(d);
+    if (st) return st;
+    return (d->H % 128 || d->I % 128) ? MOE_ERR_UNSUPPORTED : MOE_OK;
+}
+
 bool ws_ok(const void* ws, size_t have, size_t need) {
     if (need == 0) return true;
     return ws && (reinterpret_cast<uintptr_t>(ws) % kAlign) == 0 && have >= need;
@@ -269,6 +320,76 @@ int moe_testing_layer_stalled_barrier(const moe_dims* d, const uint16_t* x, cons
                                       const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                                       float* out, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream) {
     return layer_impl(d, x, logits, w_gate, w_up, w_down, out, nullptr, nullptr, ws, ws_bytes, status_dev, stream, 1);
+}
+
+// ------------------------------------------------------------------ MXFP8
+
+int moe_quantize_mxfp8(const uint16_t* src, int64_t rows, int32_t K, uint8_t* q, uint8_t* s, void* stream) {
+    if (rows < 0 || K < 32 || K % 32 || rows * (int64_t)K >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!aligned16(src) || !aligned16(q) || !s) return MOE_ERR_INVALID_ARG;
+    int st = check_device();
+    if (st) return st;
+    return launched(launch_mx_quantize(src, rows, K, q, s, (cudaStream_t)stream));
+}
+
+size_t moe_expert_ffn_mxfp8_workspace_size(const moe_dims* d) {
+    if (check_mx_dims(d) != MOE_OK) return 0;
+    return align_up(mx_ffn_scratch_bytes((long long)pairs_of(d), d->I));
+}
+
+int moe_expert_ffn_mxfp8(const moe_dims* d, const uint8_t* x_perm_q, const uint8_t* x_perm_s, const int32_t* offsets,
+                         const uint8_t* w_gate_q, const uint8_t* w_gate_s, const uint8_t* w_up_q,
+                         const uint8_t* w_up_s, const uint8_t* w_down_q, const uint8_t* w_down_s, float* y_perm,
+                         void* ws, size_t ws_bytes, int32_t* status_dev, void* stream) {
+    int st = check_mx_dims(d);
+    if (st) return st;
+    const void* ptrs[] = {x_perm_q, x_perm_s, offsets, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q, w_down_s, y_perm};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!ws_ok(ws, ws_bytes, moe_expert_ffn_mxfp8_workspace_size(d))) return MOE_ERR_WORKSPACE;
+    if ((st = check_device())) return st;
+    return launched(launch_mx_expert_ffn(x_perm_q, x_perm_s, offsets, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q,
+                                         w_down_s, y_perm, (long long)pairs_of(d), d->H, d->I, d->e1 - d->e0, ws,
+                                         status_dev, (cudaStream_t)stream));
+}
+
+size_t moe_layer_mxfp8_workspace_size(const moe_dims* d) {
+    if (check_mx_dims(d) != MOE_OK) return 0;
+    return carve_mx(d, nullptr).total;
+}
+
+int moe_layer_mxfp8(const moe_dims* d, const uint16_t* x, const float* logits, const uint8_t* w_gate_q,
+                    const uint8_t* w_gate_s, const uint8_t* w_up_q, const uint8_t* w_up_s, const uint8_t* w_down_q,
+                    const uint8_t* w_down_s, float* out, int32_t* topk_idx_opt, float* topk_w_opt, void* ws,
+                    size_t ws_bytes, int32_t* status_dev, void* stream) {
+    int st = check_mx_dims(d);
+    if (st) return st;
+    const void* ptrs[] = {x, logits, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q, w_down_s, out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if ((topk_idx_opt && !aligned16(topk_idx_opt)) || (topk_w_opt && !aligned16(topk_w_opt)))
+        return MOE_ERR_INVALID_ARG;
+    if (!ws_ok(ws, ws_bytes, carve_mx(d, nullptr).total)) return MOE_ERR_WORKSPACE;
+    if ((st = check_device())) return st;
+    MxLayerWs w = carve_mx(d, ws);
+    int32_t* idx = topk_idx_opt ? topk_idx_opt : w.topk_idx;
+    float* wt = topk_w_opt ? topk_w_opt : w.topk_w;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int n = d->e1 - d->e0;
+    int32_t* hist = static_cast<int32_t*>(w.dispatch_ws);
+    if (cudaMemsetAsync(hist, 0, w.dispatch_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_route_hist(logits, d->T, d->E, d->k, idx, wt, status_dev, hist, dispatch_chunk_tokens(d->T), d->e0, n,
+                          s) != cudaSuccess ||
+        launch_mx_quantize(x, d->T, d->H, w.xq, w.xs, s) != cudaSuccess ||
+        launch_dispatch_place(x, idx, hist, d->T, d->H, d->k, d->e0, d->e1, w.counts, w.offsets, w.row_pair,
+                              w.pair_row, nullptr, s) != cudaSuccess ||
+        launch_mx_gather(w.xq, w.xs, d->T, d->H, d->k, w.pair_row, w.xpq, w.xps, s) != cudaSuccess ||
+        launch_mx_expert_ffn(w.xpq, w.xps, w.offsets, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q, w_down_s,
+                             w.y_perm, (long long)pairs_of(d), d->H, d->I, n, w.ffn_ws, status_dev, s) != cudaSuccess ||
+        launch_combine(w.y_perm, w.pair_row, wt, d->T, d->H, d->k, out, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 }  // extern "C"

@@ -337,8 +337,10 @@ cudaError_t launch_dispatch_place(const uint16_t* x, const int32_t* topk_idx, co
     dispatch_place_kernel<<<nchunks, kPlaceThreads, 0, s>>>(topk_idx, hist, nchunks, chunk, T, k, e0, e1 - e0, counts,
                                                             offsets, row_pair, pair_row);
     // the row copy wants far more CTAs than there are chunks: one CTA per token
-    dispatch_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), T, H / 8, k, pair_row,
-                                             reinterpret_cast<uint4*>(x_perm));
+    // (x_perm NULL: the caller copies the rows itself, e.g. in another format)
+    if (x_perm)
+        dispatch_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), T, H / 8, k, pair_row,
+                                                 reinterpret_cast<uint4*>(x_perm));
     return cudaGetLastError();
 }
 

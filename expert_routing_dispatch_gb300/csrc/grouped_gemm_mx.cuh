@@ -1,0 +1,424 @@
+// grouped_gemm_mx.cuh -- the grouped expert GEMMs with MXFP8 operands on the
+// block-scaled tcgen05 tensor cores (kind::mxf8f6f4).
+//
+// "Hosting Qwen on Blackwell", section "MoE GEMM": the deployed expert GEMMs run
+// in MXFP8.  Operands are OCP MX v1.0 MXFP8: E4M3 codes (one byte per element,
+// K-major) and one UE8M0 scale per 32 elements along K.  The scales of a row are
+// read as 32-bit words, four per 128-element k-block, so K is a multiple of 128.
+//
+//   gate/up : acc[128 x 192] = x[rows] . [W_gate rows n..n+95 ; W_up rows n..n+95]^T
+//             epilogue h = silu(acc[:, 0:96]) * acc[:, 96:192] (fp32), quantised to
+//             MXFP8 along I (each 32-column chunk of a row is one MX block)
+//   down    : acc[128 x 192] = h[rows] . W_down[e][n..n+191]^T  ->  y_perm (fp32)
+//
+// One MMA instruction covers K = 32 (one scale per row of A and column of B); a
+// 128-byte k-block is four of them, scale ID j picking byte j of each scale word.
+// Block-scale factors live in tensor memory: for M = 128 the scale of row m is at
+// lane m, column m / 32 of the A slot; the scale of B row n at lane n % 32, column
+// n / 32 of the B slot, repeated in every 32-lane quadrant (each quadrant of
+// accumulator rows reads the B scales from its own lanes).
+//
+// CTA = 10 warps: warp 0 issues the TMA loads of the E4M3 tiles into a 4-stage
+// ring; warp 1 owns TMEM (two 192-column accumulators and four 12-column scale
+// slots) and one of its threads issues the MMAs; warps 2..5 run the epilogue;
+// warps 6..9 (one per TMEM lane quadrant) gather each stage's scale words and
+// write them into the stage's scale slot with tcgen05.st.  Every wait is bounded.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+namespace mx {
+
+constexpr int BM = 128, BN = 192, BKB = 128;  // k-block: 128 E4M3 = 128 bytes per row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BKB;              // 16 KB
+constexpr int B_BYTES = BN * BKB;              // 24 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 40 KB
+constexpr int NUM_THREADS = 320;
+constexpr int ACC_COLS = BN;
+constexpr int SF_COL0 = 2 * ACC_COLS;  // first scale slot column (384)
+constexpr int SF_SLOT = 12;            // columns per slot: 4 for A, 6 (of 8) for B
+constexpr int TMEM_COLS = 512;
+constexpr int MAX_LOCAL = 1024;
+constexpr long long WAIT_LIMIT = 1ll << 31;
+
+enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
+
+struct Ctl {
+    alignas(128) uint4 stage[4][32 * 8];  // down epilogue: 32-row x 128-byte fp32 staging per warp
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t sffull[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int tile_start[MAX_LOCAL + 1];
+    int row_off[MAX_LOCAL + 1];
+};
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
+static_assert(SMEM_BYTES <= 232448, "MX GEMM exceeds the 227 KB shared-memory limit");
+
+struct Args {
+    void* out;               // gate/up: h codes uint8 [rows, I]; down: y_perm fp32 [rows, H]
+    uint8_t* out_s;          // gate/up: h scales uint8 [rows, I/32]
+    const uint32_t* a_s;     // token scale words [a_rows, K/128]
+    const uint32_t* b0_s;    // W_gate (gate/up) or W_down scale words [n * w_rows, K/128]
+    const uint32_t* b1_s;    // W_up scale words (gate/up)
+    long long a_rows;        // rows of the token buffers
+    int32_t* status;
+    int n;                   // local experts
+    int kblocks;             // K / 128
+    int ntiles_n;            // n-tiles per expert
+    int out_cols;            // I (gate/up) or H (down)
+    int w_rows;              // weight rows per expert (I or H)
+    int n_step;              // output columns per n-tile: 96 (gate/up) or 192 (down)
+};
+
+struct TileCoord {
+    int e, mt, nt, cnt;
+};
+
+__device__ __forceinline__ uint32_t ring_base(uint8_t* raw) { return (smem_u32(raw) + 1023u) & ~1023u; }
+__device__ __forceinline__ Ctl& ctl_of(uint8_t* raw) {
+    const uint32_t b = ring_base(raw);
+    return *reinterpret_cast<Ctl*>(raw + (b - smem_u32(raw)) + (size_t)STAGES * STAGE_BYTES);
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B, UE8M0 scales:
+//   bits 4-5 B scale ID, 7-9 A format (0 = E4M3), 10-12 B format, 17-22 N >> 3,
+//   23 scale type (1 = UE8M0), 24-28 M >> 4, 29-30 A scale ID
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
+    return ((uint32_t)sf_id << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+           ((uint32_t)sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// UE8M0 code of a block whose largest magnitude is amax (OCP MX: floor(log2(amax))
+// - 8 + 127, clamped to [0, 254]; 0 for amax = 0 or below the normal range)
+__device__ __forceinline__ uint32_t mx_scale_code(float amax) {
+    const int eb = (int)((__float_as_uint(amax) >> 23) & 0xffu);  // amax >= 0
+    const int c = eb - 8;                                           // floor(log2) - 8 + 127
+    return (uint32_t)(c < 0 ? 0 : c > 254 ? 254 : c);
+}
+// two floats -> two E4M3 codes (round to nearest even, saturating at 448), lo in bits 0..7
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// 32 fp32 values of one MX block -> 32 E4M3 codes (8 words) and the scale code
+__device__ __forceinline__ uint32_t mx_quantize32(const float (&v)[32], uint32_t (&w)[8]) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t code = mx_scale_code(amax);
+    const float inv = __uint_as_float((254u - code) << 23);  // 2^(127 - code): exact
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) | (e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+    return code;
+}
+
+__device__ __forceinline__ void init(Ctl& c) {
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&c.full[s]), 1);
+            mbar_init(smem_u32(&c.empty[s]), 1);
+            mbar_init(smem_u32(&c.sffull[s]), 4);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&c.tfull[a]), 1);
+            mbar_init(smem_u32(&c.tempty[a]), 4);
+        }
+        mbar_init(smem_u32(&c.drain), 1);
+        c.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+}
+
+// warp 0: tile_start from row_off
+__device__ __forceinline__ void build_tile_table(Ctl& c, int n, int ntiles_n) {
+    if ((threadIdx.x >> 5) != 0) return;
+    const int lane = threadIdx.x & 31;
+    int carry = 0;
+    for (int b0 = 0; b0 < n; b0 += 32) {
+        const int e = b0 + lane;
+        int v = 0;
+        if (e < n) v = ((c.row_off[e + 1] - c.row_off[e] + BM - 1) / BM) * ntiles_n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (e < n) c.tile_start[e + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) c.tile_start[0] = 0;
+}
+
+__device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_hint, TileCoord& tc) {
+    if (tile >= c.tile_start[n]) return false;
+    int e = e_hint;
+    while (c.tile_start[e + 1] <= tile) ++e;
+    e_hint = e;
+    const int cnt = c.row_off[e + 1] - c.row_off[e];
+    const int mtiles = (cnt + BM - 1) / BM;
+    const int local = tile - c.tile_start[e];
+    tc.e = e;
+    tc.nt = local / mtiles;
+    tc.mt = local - tc.nt * mtiles;
+    tc.cnt = cnt;
+    return true;
+}
+
+// One GEMM over all tiles; every thread of the CTA calls it and plays its role.
+//   tmA: token codes [a_rows, K], 128-row boxes; tmB0 / tmB1: weight codes with
+//   boxes of n_step rows (gate/up: W_gate / W_up) or BN rows (down: W_down twice)
+template <int MODE>
+__device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tmA, const CUtensorMap* tmB0,
+                                    const CUtensorMap* tmB1, const Args& args) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = args.n;
+    volatile int* abort_flag = &c.abort_flag;
+    auto a_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES); };
+    auto b_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES + A_BYTES); };
+    int e_hint = 0;
+    TileCoord tc;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            int g = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
+                const int a_row = c.row_off[tc.e] + tc.mt * BM;
+                const int b_row = tc.e * args.w_rows + tc.nt * args.n_step;
+                for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
+                    const int s = g % STAGES, r = g / STAGES;
+                    if (!mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag, args.status,
+                                           WAIT_LIMIT)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&c.full[s]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
+                    tma_load_2d(a_addr(s), tmA, kb * BKB, a_row, fb, pol);
+                    if (MODE == MODE_GATEUP) {  // [96 gate rows | 96 up rows]
+                        tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
+                        tma_load_2d(b_addr(s) + (uint32_t)(BN / 2) * BKB, tmB1, kb * BKB, b_row, fb, pol);
+                    } else {
+                        tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            int g = 0, it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && !*abort_flag && next_tile(c, n, tile, e_hint, tc);
+                 tile += gridDim.x, ++it) {
+                const int acc = it & 1, use = it >> 1;
+                if (!mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag, args.status, WAIT_LIMIT))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * ACC_COLS);
+                for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
+                    const int s = g % STAGES, r = g / STAGES;
+                    if (!mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status, WAIT_LIMIT) ||
+                        !mbar_wait_bounded(smem_u32(&c.sffull[s]), r & 1, abort_flag, args.status, WAIT_LIMIT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa = c.tmem_base + (uint32_t)(SF_COL0 + s * SF_SLOT);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_mxf8(d_tmem, sdesc_k_swz<128>(a_addr(s) + j * 32), sdesc_k_swz<128>(b_addr(s) + j * 32),
+                                 idesc_mxf8(BM, BN, j), sfa, sfa + 4, (kb | j) != 0);
+                    tc_commit(smem_u32(&c.empty[s]));
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&c.tfull[acc]));
+            }
+        }
+    } else if (warp >= 6) {
+        // ================= scale-factor warps (lane quadrant q = warp % 4) =================
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const long long b_total = (long long)n * args.w_rows;
+        int g = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
+            const long long a_row = (long long)c.row_off[tc.e] + tc.mt * BM + lane;
+            const long long b_row = (long long)tc.e * args.w_rows + tc.nt * args.n_step + lane;
+            for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
+                const int s = g % STAGES, r = g / STAGES;
+                uint32_t va[4], vb[6];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const long long row = a_row + 32 * i;
+                    va[i] = row < args.a_rows ? __ldg(args.a_s + row * args.kblocks + kb) : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 6; ++i) {
+                    long long row;
+                    const uint32_t* src;
+                    if (MODE == MODE_GATEUP) {  // columns 0-2: gate rows, 3-5: up rows of the same h columns
+                        row = b_row + 32 * (i % 3);
+                        src = i < 3 ? args.b0_s : args.b1_s;
+                    } else {
+                        row = b_row + 32 * i;
+                        src = args.b0_s;
+                    }
+                    vb[i] = row < b_total ? __ldg(src + row * args.kblocks + kb) : 0u;
+                }
+                if (!mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag, args.status, WAIT_LIMIT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t slot = c.tmem_base + lane_off + (uint32_t)(SF_COL0 + s * SF_SLOT);
+                tmem_st4(slot, va[0], va[1], va[2], va[3]);
+                tmem_st4(slot + 4, vb[0], vb[1], vb[2], vb[3]);
+                tmem_st2(slot + 8, vb[4], vb[5]);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&c.sffull[s]));
+            }
+        }
+    } else {
+        // ================= epilogue (warps 2..5, TMEM lane quarter q = warp % 4) =================
+        const int q = warp & 3;
+        int it = 0;
+        for (int tile = blockIdx.x; !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++it) {
+            const int acc = it & 1, use = it >> 1;
+            if (!mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status, WAIT_LIMIT)) break;
+            tc_fence_after();
+            const int row0_in_e = tc.mt * BM + q * 32;
+            const long long grow0 = (long long)c.row_off[tc.e] + row0_in_e;
+            const uint32_t taddr = c.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+            const int col0 = tc.nt * args.n_step;
+            if (MODE == MODE_GATEUP) {
+                // thread = one token row; 32 h columns per chunk = one MX block
+                uint8_t* hq = static_cast<uint8_t*>(args.out);
+                const bool row_ok = row0_in_e + lane < tc.cnt;
+                const long long grow = grow0 + lane;
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 2; cc += 32) {
+                    uint32_t g0[16], g1[16], u0[16], u1[16];
+                    tmem_ld16(taddr + cc, g0);
+                    tmem_ld16(taddr + cc + 16, g1);
+                    tmem_ld16(taddr + BN / 2 + cc, u0);
+                    tmem_ld16(taddr + BN / 2 + cc + 16, u1);
+                    tmem_ld_wait();
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float a0 = __uint_as_float(g0[i]), b0 = __uint_as_float(u0[i]);
+                        const float a1 = __uint_as_float(g1[i]), b1 = __uint_as_float(u1[i]);
+                        h[i] = a0 / (1.f + __expf(-a0)) * b0;
+                        h[16 + i] = a1 / (1.f + __expf(-a1)) * b1;
+                    }
+                    uint32_t w[8];
+                    const uint32_t code = mx_quantize32(h, w);
+                    if (row_ok && col0 + cc < args.out_cols) {
+                        uint4* dst = reinterpret_cast<uint4*>(hq + grow * args.out_cols + col0 + cc);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        args.out_s[grow * (args.out_cols / 32) + (col0 + cc) / 32] = (uint8_t)code;
+                    }
+                }
+            } else {
+                // 32 fp32 columns per chunk: 128 B per row, 8 slots; slot = piece ^ (row & 7)
+                float* out = static_cast<float*>(args.out);
+                uint4* st = c.stage[q];
+#pragma unroll 1
+                for (int cc = 0; cc < BN; cc += 32) {
+                    uint32_t v0[16], v1[16];
+                    tmem_ld16(taddr + cc, v0);
+                    tmem_ld16(taddr + cc + 16, v1);
+                    tmem_ld_wait();
+                    const int sw = lane & 7;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        st[lane * 8 + (j ^ sw)] = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+                        st[lane * 8 + ((j + 4) ^ sw)] =
+                            make_uint4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
+                    }
+                    __syncwarp();
+                    if (col0 + cc < args.out_cols) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int r = i * 4 + (lane >> 3), piece = lane & 7;
+                            const uint4 v = st[r * 8 + (piece ^ (r & 7))];
+                            if (row0_in_e + r < tc.cnt)
+                                *reinterpret_cast<uint4*>(out + (grow0 + r) * args.out_cols + col0 + cc + 4 * piece) = v;
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&c.tempty[acc]));
+        }
+        // the h codes are read later through TMA (async proxy)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+}
+
+// After a __syncthreads: drain the MMAs (bounded), free TMEM.  Every load the
+// producer issued was consumed by an MMA unless a wait gave up; then the loads
+// still land within the bounded drain below.
+__device__ __forceinline__ void teardown(Ctl& c, int32_t* status) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 1) {
+        if (lane == 0) {
+            tc_commit(smem_u32(&c.drain));
+            volatile int never = 0;
+            mbar_wait_bounded(smem_u32(&c.drain), 0, &never, status, WAIT_LIMIT);
+            if (c.abort_flag) {  // copies may still be in flight: let them land
+                const long long t0 = clock64();
+                while (clock64() - t0 < (1ll << 20)) {
+                }
+            }
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(c.tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace mx
+}  // namespace moe

@@ -214,6 +214,55 @@ int moe_testing_layer_stalled_barrier(const moe_dims* d, const uint16_t* x, cons
                                       const uint16_t* w_down, float* out, void* ws, size_t ws_bytes,
                                       int32_t* status_dev, void* stream);
 
+/*
+ * MXFP8 expert FFN ("MoE GEMM" section: the deployed expert GEMMs run in MXFP8).
+ * The pages name the format only; it is read as OCP Microscaling (MX) v1.0 MXFP8:
+ *   - an MXFP8 matrix [rows, K] is q uint8 [rows, K] (E4M3 codes: sign, 4 exponent
+ *     bits with bias 7, 3 mantissa bits, no infinities, 0x7f/0xff NaN) and
+ *     s uint8 [rows, K/32] (UE8M0 codes: the scale of elements 32b..32b+31 of a row
+ *     is 2^(s[row, b] - 127));
+ *   - quantisation of a block: X = 2^(floor(log2(amax)) - 8) (code 0 for a zero
+ *     block, clamped to [0, 254]), each element = v / X rounded to the nearest E4M3
+ *     value, ties to even, saturating at +-448.
+ * The MX GEMMs accumulate in fp32 on the block-scaled tcgen05 tensor cores
+ * (kind::mxf8f6f4); h = silu(g) * u is computed in fp32 and quantised to MXFP8
+ * along I before the down GEMM; y_perm and the layer output are fp32.
+ * Limits on top of moe_dims': H and I multiples of 128 (else MOE_ERR_UNSUPPORTED).
+ * All q and s pointers must be 16-byte aligned.
+ */
+
+/* q, s = MXFP8 of the bf16 matrix src [rows, K] (K a multiple of 32).  Bit-exact
+ * with the definition above. */
+int moe_quantize_mxfp8(const uint16_t* src, int64_t rows, int32_t K, uint8_t* q, uint8_t* s, void* stream);
+
+/*
+ * moe_expert_ffn with MXFP8 operands: x_perm (q [T*k, H], s [T*k, H/32]) grouped
+ * by `offsets` as moe_dispatch makes them; w_gate, w_up (q [n, I, H], s [n, I, H/32])
+ * and w_down (q [n, H, I], s [n, H, I/32]), e.g. from moe_quantize_mxfp8.
+ *   y_perm fp32 [T*k, H] out (rows >= R untouched)
+ *   ws >= moe_expert_ffn_mxfp8_workspace_size(d) bytes, 256-byte aligned; it holds
+ *   the quantised h: codes [T*k, I] at offset 0, then scales [T*k, I/32] at the
+ *   next multiple of 256 bytes
+ */
+size_t moe_expert_ffn_mxfp8_workspace_size(const moe_dims* d);
+int moe_expert_ffn_mxfp8(const moe_dims* d, const uint8_t* x_perm_q, const uint8_t* x_perm_s, const int32_t* offsets,
+                         const uint8_t* w_gate_q, const uint8_t* w_gate_s, const uint8_t* w_up_q,
+                         const uint8_t* w_up_s, const uint8_t* w_down_q, const uint8_t* w_down_s, float* y_perm,
+                         void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * The whole local layer with MXFP8 expert weights: route, dispatch (x quantised to
+ * MXFP8 once per token, rows gathered in that format), the MXFP8 expert FFN and the
+ * weighted fp32 combine into out fp32 [T, H].  Always the split kernels (no fused
+ * decode launch).  Routing, counts, offsets and the permutation are those of
+ * moe_layer.  ws >= moe_layer_mxfp8_workspace_size(d) bytes, 256-byte aligned.
+ */
+size_t moe_layer_mxfp8_workspace_size(const moe_dims* d);
+int moe_layer_mxfp8(const moe_dims* d, const uint16_t* x, const float* logits, const uint8_t* w_gate_q,
+                    const uint8_t* w_gate_s, const uint8_t* w_up_q, const uint8_t* w_up_s, const uint8_t* w_down_q,
+                    const uint8_t* w_down_s, float* out, int32_t* topk_idx_opt, float* topk_w_opt, void* ws,
+                    size_t ws_bytes, int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

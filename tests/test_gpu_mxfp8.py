@@ -1,0 +1,195 @@
+"""GPU parity of the MXFP8 expert path ("MoE GEMM" section of "Hosting Qwen on
+Blackwell": the deployed expert GEMMs run in MXFP8, read as OCP MX v1.0 MXFP8)
+against the oracle, through the C ABI.
+
+Bars:
+- quantisation (moe_quantize_mxfp8) is bit-exact: E4M3 codes and UE8M0 scales;
+- h (quantised in the gate/up epilogue from fp32 values): every element within one
+  E4M3 step of the oracle's fp64 h at the GPU's block scale, plus 1e-4 of the
+  row's largest |h| for the fp32 arithmetic; codes that differ from the oracle's
+  quantisation of its own h (rounding-boundary flips) stay rare (< 2%);
+- the down GEMM alone (the oracle fed the GPU's own quantised h): within 1e-3 *
+  RMS, i.e. fp32 accumulation (a wrong scale anywhere would be a factor of 2);
+- the expert FFN and the layer against the oracle's own MXFP8 pipeline: within
+  2e-2 * RMS; routing bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_helpers import dev, host, inputs, oracle_routing, rel_err, sample_rows, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = ["tiny", "decode", "prefill_ep_rank", "skewed_rank0"]
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import torch
+
+    import expert_routing_dispatch_gb300 as m
+
+    assert torch.cuda.is_available()
+    m.lib()
+    return m
+
+
+_wcache = {}
+
+
+def mx_weights(name):
+    """oracle MXFP8 of the config's weights: (q, s) per matrix, shaped like the bf16 weights"""
+    if name not in _wcache:
+        cfg, inp = inputs(name)
+        out = {}
+        for key in ("w_gate", "w_up", "w_down"):
+            w = inp[key]
+            q, s = oracle.mxfp8_quantize(w.reshape(-1, w.shape[-1]))
+            out[key] = (q.reshape(w.shape), s.reshape(w.shape[:-1] + (w.shape[-1] // 32,)))
+        _wcache[name] = out
+    return _wcache[name]
+
+
+def e4m3_step(a):
+    """spacing of E4M3 values at magnitude a (a = |value| / block scale)"""
+    a = np.maximum(np.asarray(a, np.float64), 2.0 ** -6)
+    return 2.0 ** (np.floor(np.log2(a)) - 3)
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill_ep_rank"])
+def test_quantize_bit_exact(moe, name):
+    import torch
+
+    cfg, inp = inputs(name)
+    for key in ("x", "w_down"):
+        a = inp[key].reshape(-1, inp[key].shape[-1])[:4096]
+        rows, K = a.shape
+        q = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+        s = torch.empty((rows, K // 32), dtype=torch.uint8, device="cuda")
+        moe.moe_quantize_mxfp8(dev(a), rows, K, q, s)
+        torch.cuda.synchronize()
+        rq, rs = oracle.mxfp8_quantize(a)
+        assert np.array_equal(host(q), rq) and np.array_equal(host(s), rs), key
+
+
+def test_quantize_special_values(moe):
+    import torch
+
+    # zero block, ties, saturation, signed zero, subnormal codes, a block near the bottom of the scale range
+    vals = np.zeros((4, 32), np.float32)
+    vals[1, :6] = [256.0, 17.0, 19.0, -17.0, -(2.0 ** -100), 500.0]
+    vals[2] = np.linspace(-1.0, 1.0, 32) * 2.0 ** -8
+    vals[2, 0] = 448.0 * 2.0 ** -8
+    vals[3] = np.linspace(0, 1, 32) * 2.0 ** -118
+    a = synth.f32_to_bf16(vals)
+    q = torch.empty((4, 32), dtype=torch.uint8, device="cuda")
+    s = torch.empty((4, 1), dtype=torch.uint8, device="cuda")
+    moe.moe_quantize_mxfp8(dev(a), 4, 32, q, s)
+    torch.cuda.synchronize()
+    rq, rs = oracle.mxfp8_quantize(a)
+    assert np.array_equal(host(q), rq) and np.array_equal(host(s), rs)
+
+
+def run_ffn(moe, name):
+    import torch
+
+    cfg, inp = inputs(name)
+    T, H, I, E, k, e0, e1 = synth.dims_of(cfg)
+    _, _, d = oracle_routing(name)
+    P, R = T * k, d["R"]
+    xq_t, xs_t = oracle.mxfp8_quantize(inp["x"])
+    xq = np.zeros((P, H), np.uint8)
+    xs = np.zeros((P, H // 32), np.uint8)
+    xq[:R] = xq_t[d["row_pair"] // k]
+    xs[:R] = xs_t[d["row_pair"] // k]
+    w = mx_weights(name)
+    dw = {key: (dev(q), dev(s)) for key, (q, s) in w.items()}
+    y = torch.full((P, H), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = moe.alloc_workspace(moe.moe_expert_ffn_mxfp8_workspace_size(cfg))
+    moe.moe_expert_ffn_mxfp8(cfg, dev(xq), dev(xs), dev(d["offsets"]), dw["w_gate"], dw["w_up"], dw["w_down"], y, ws,
+                             status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    hq_off = (P * I + 255) // 256 * 256
+    wsh = host(ws)
+    hq = wsh[:P * I].reshape(P, I)
+    hs = wsh[hq_off:hq_off + P * (I // 32)].reshape(P, I // 32)
+    return cfg, d, xq, xs, w, host(y), hq, hs
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_mx_expert_ffn(moe, name):
+    cfg, d, xq, xs, w, y, hq, hs = run_ffn(moe, name)
+    R = d["R"]
+    rows = sample_rows(d["offsets"], extra=48 if R > 4096 else R)
+    if rows.size == 0:
+        return
+    args = (xq, xs, d["offsets"], w["w_gate"], w["w_up"], w["w_down"], rows)
+    y_own, h64, hq_o, hs_o = oracle.expert_ffn_mxfp8_rowlist(*args, want_h=True)
+    y_gpu_h = oracle.expert_ffn_mxfp8_rowlist(*args, h_in=(hq[rows], hs[rows]))
+    # h: one E4M3 step at the GPU's block scale (+ fp32 arithmetic)
+    hg = oracle.mxfp8_dequantize(hq[rows], hs[rows])
+    X = np.repeat(2.0 ** (hs[rows].astype(np.float64) - 127), 32, axis=1)
+    step = e4m3_step(np.maximum(np.abs(hg), np.abs(h64)) / X) * X
+    sat = np.maximum(np.abs(h64) - 448.0 * X, 0.0)
+    tol = 1.01 * step + sat + 1e-4 * np.abs(h64).max(axis=1, keepdims=True)
+    assert (np.abs(hg - h64) <= tol).all(), float((np.abs(hg - h64) / tol).max())
+    flips = float(np.mean(hq[rows] != hq_o))
+    # the down GEMM alone, and the whole FFN against the oracle's own MXFP8 pipeline
+    e_down, rms_down = rel_err(y[rows], y_gpu_h)
+    e_all, rms_all = rel_err(y[rows], y_own)
+    print(f"PARITY mxfp8 ffn {cfg['name']} h code flips {flips:.4%}, down-only max/RMS {e_down / rms_down:.2e}, "
+          f"ffn max/RMS {e_all / rms_all:.2e}")
+    assert flips < 0.02
+    assert e_down <= 1e-3 * rms_down
+    assert e_all <= 2e-2 * rms_all
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill_ep_rank", "skewed"])
+def test_mx_layer(moe, name):
+    import torch
+
+    cfg, inp = inputs(name)
+    T, H, I, E, k, e0, e1 = synth.dims_of(cfg)
+    idx_o, w_o, d = oracle_routing(name)
+    w = mx_weights(name)
+    dw = {key: (dev(q), dev(s)) for key, (q, s) in w.items()}
+    out = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    idx = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = moe.alloc_workspace(moe.moe_layer_mxfp8_workspace_size(cfg))
+    moe.moe_layer_mxfp8(cfg, dev(inp["x"]), dev(inp["logits"]), dw["w_gate"], dw["w_up"], dw["w_down"], out, ws,
+                        topk_idx=idx, topk_w=wt, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(host(idx), idx_o)
+    toks = sample_tokens(T, 48)
+    # oracle: MXFP8 FFN of every local slot of the sampled tokens, combined in slot order
+    xq_t, xs_t = oracle.mxfp8_quantize(inp["x"])
+    P = T * k
+    pr = d["pair_row"]
+    rows = np.unique(np.array([pr[t * k + j] for t in toks for j in range(k) if pr[t * k + j] >= 0], np.int64))
+    got = host(out)[toks]
+    if rows.size == 0:
+        assert (got == 0).all()
+        return
+    xq = np.zeros((P, H), np.uint8)
+    xs = np.zeros((P, H // 32), np.uint8)
+    xq[:d["R"]] = xq_t[d["row_pair"] // k]
+    xs[:d["R"]] = xs_t[d["row_pair"] // k]
+    y_rows = oracle.expert_ffn_mxfp8_rowlist(xq, xs, d["offsets"], w["w_gate"], w["w_up"], w["w_down"], rows)
+    y_perm = np.zeros((P, H), np.float32)
+    y_perm[rows] = y_rows.astype(np.float32)
+    ref = oracle.combine_tokens(y_perm, pr, w_o.astype(np.float32), tokens=toks)
+    err, rms = rel_err(got, ref)
+    # context only: the bf16 oracle of the same tokens
+    st, ref16 = oracle.moe_layer_tokens(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], k, e0, e1,
+                                        tokens=toks)
+    e16, rms16 = rel_err(got, ref16)
+    print(f"PARITY mxfp8 layer {name} max|gpu-oracle_mx|/RMS = {err / rms:.3e} (vs the bf16 oracle: "
+          f"{e16 / rms16:.3e})")
+    assert err <= 2e-2 * rms
