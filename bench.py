@@ -50,6 +50,9 @@ def parse():
     p.add_argument("--config", default="prefill_ep_rank")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--precision", choices=["bf16", "mxfp8"], default="bf16",
+                   help="expert GEMM operands: bf16 (the workload's statement), or MXFP8 expert weights and "
+                        "activations (moe_layer_mxfp8; weights quantised on the device before timing)")
     return p.parse_args()
 
 
@@ -284,20 +287,40 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    lws = moe.alloc_workspace(moe.moe_workspace_size(dims), dev)
-    fused = P <= moe.FUSED_MAX_PAIRS
+    mx = args.precision == "mxfp8"
+    if mx:
+        # MXFP8 expert weights, quantised once on the device (outside every timed region)
+        u8 = torch.uint8
+        wq = {}
+        for key, w_, rows_, K_ in (("g", wg, n * I, H), ("u", wu, n * I, H), ("d", wd, n * H, I)):
+            q_ = torch.empty((rows_, K_), dtype=u8, device=dev)
+            s_ = torch.empty((rows_, K_ // 32), dtype=u8, device=dev)
+            moe.moe_quantize_mxfp8(w_, rows_, K_, q_, s_, stream=sh)
+            wq[key] = (q_, s_)
+        torch.cuda.synchronize()
+        lws = moe.alloc_workspace(moe.moe_layer_mxfp8_workspace_size(dims), dev)
+    else:
+        lws = moe.alloc_workspace(moe.moe_workspace_size(dims), dev)
+
+    def run_layer(x_, lg_, out_, **kw):
+        if mx:
+            moe.moe_layer_mxfp8(dims, x_, lg_, wq["g"], wq["u"], wq["d"], out_, lws, status=status, stream=sh, **kw)
+        else:
+            moe.moe_layer(dims, x_, lg_, wg, wu, wd, out_, lws, status=status, stream=sh, **kw)
+
+    fused = P <= moe.FUSED_MAX_PAIRS and not mx
     # the timed step: one moe_layer call (decode-sized: one persistent launch; else
     # route + dispatch place/gather + gate/up + down + combine)
-    names = ["layer_fused" if fused else "layer"]
-    launches_per_step = 1 if fused else 6
+    names = ["layer_fused" if fused else "layer_mxfp8" if mx else "layer"]
+    # route, place, gather, gate/up, down, combine (+ the quantisation of x for MXFP8)
+    launches_per_step = 1 if fused else 7 if mx else 6
 
     def step(evs):
         evs[0].record(stream)
-        moe.moe_layer(dims, x, lg, wg, wu, wd, out, lws, topk_idx=topk_idx, topk_w=topk_w, status=status,
-                      stream=sh)
+        run_layer(x, lg, out, topk_idx=topk_idx, topk_w=topk_w)
         evs[1].record(stream)
 
-    if not fused:
+    if not fused and not mx:
         # breakdown loop (not the headline): the same work as separate entry calls
         bnames = ["route", "dispatch", "gate_up", "down", "combine"]
 
@@ -340,7 +363,28 @@ def run_ours(args):
     step_ms = [evs[0].elapsed_time(evs[-1]) for evs in all_evs]
     t_step = sum(step_ms) / len(step_ms)
     kern_ms = {names[0]: t_step}
-    if not fused:
+    if mx:
+        # the MXFP8 expert FFN alone (both GEMMs, moe_expert_ffn_mxfp8) on this run's grouped rows
+        moe.moe_route(dims, lg, topk_idx, topk_w, status, stream=sh)
+        moe.moe_dispatch(dims, x, topk_idx, counts, offsets, row_pair, pair_row, x_perm, dws, stream=sh)
+        xpq = torch.empty((P, H), dtype=torch.uint8, device=dev)
+        xps = torch.empty((P, H // 32), dtype=torch.uint8, device=dev)
+        moe.moe_quantize_mxfp8(x_perm, P, H, xpq, xps, stream=sh)
+        fws = moe.alloc_workspace(moe.moe_expert_ffn_mxfp8_workspace_size(dims), dev)
+        ts = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            moe.moe_expert_ffn_mxfp8(dims, xpq, xps, offsets, wq["g"], wq["u"], wq["d"], y_perm, fws, status=status,
+                                     stream=sh)
+            a1.record(stream)
+            a1.synchronize()
+            if i >= args.warmup:
+                ts.append(a0.elapsed_time(a1))
+        kern_ms["ffn_mxfp8"] = sum(ts) / len(ts)
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
+    if not fused and not mx:
         # per-kernel breakdown from the entry-by-entry loop (same warm-up, flush and step count)
         b_evs = []
         for i in range(args.warmup + args.steps):
@@ -381,7 +425,7 @@ def run_ours(args):
     def serial_step():
         x_d[0].copy_(x_h, non_blocking=True)
         lg_d[0].copy_(lg_h, non_blocking=True)
-        moe.moe_layer(dims, x_d[0], lg_d[0], wg, wu, wd, out_d[0], lws, status=status, stream=sh)
+        run_layer(x_d[0], lg_d[0], out_d[0])
         out_h[0].copy_(out_d[0], non_blocking=True)
 
     def pipelined(steps):
@@ -398,7 +442,7 @@ def run_ours(args):
             stream.wait_event(ev_in[b])
             if i >= 2:
                 stream.wait_event(ev_out[b])  # download i-2 has read out_d[b]
-            moe.moe_layer(dims, x_d[b], lg_d[b], wg, wu, wd, out_d[b], lws, status=status, stream=sh)
+            run_layer(x_d[b], lg_d[b], out_d[b])
             ev_comp[b].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[b])
@@ -447,6 +491,16 @@ def run_ours(args):
                     "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
                     "traffic": recorded_traffic("moe_layer_fused", args.config),
                     "algorithmic_bytes_per_launch": alg_bytes}
+    elif mx:
+        # both MXFP8 grouped GEMMs against the fp8 tensor peak: the measured bf16 peak x 2
+        # (the nominal dense ratio, 4.5 / 2.25 PFLOP/s)
+        fp8_peak = 2.0 * peaks["bf16_tflops"]
+        achieved = flop_layer / (kern_ms["ffn_mxfp8"] * 1e-3) / 1e12 if R else 0.0
+        roofline = {"kernel": "grouped_ffn_mx_kernel gate/up + down (tcgen05 kind::mxf8f6f4 block-scaled)",
+                    "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp8_peak, "peak_source": f"{peak_src} bf16 burst x 2 (nominal fp8 ratio)",
+                    "traffic": recorded_traffic("grouped_ffn_mx", args.config),
+                    "algorithmic_flop_per_launch": flop_layer}
     else:
         achieved = flop_gate_up / (kern_ms["gate_up"] * 1e-3) / 1e12 if R else 0.0
         roofline = {"kernel": "grouped_ffn gate/up (tcgen05, SiLU*up epilogue)", "bound": "tensor",
@@ -454,7 +508,7 @@ def run_ours(args):
                     "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
                     "traffic": recorded_traffic("grouped_gemm_gate_up", args.config),
                     "algorithmic_flop_per_launch": flop_gate_up}
-    gemm_ms = kern_ms["layer_fused"] if fused else kern_ms["gate_up"] + kern_ms["down"]
+    gemm_ms = kern_ms["layer_fused"] if fused else kern_ms["ffn_mxfp8"] if mx else kern_ms["gate_up"] + kern_ms["down"]
     line = {
         "metric": METRIC,
         "value": job_throughput(world, T, t_step_max),
@@ -466,9 +520,9 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "mxfp8 (e4m3, ue8m0 block-32 scales; fp32 accumulate)" if mx else "bf16",
         "data": "synthetic (seeded counter-based generator; random-init weights)",
-        "config": workload_config(cfg, R),
+        "config": dict(workload_config(cfg, R), **({"precision": "mxfp8"} if mx else {})),
         "e2e": {"value": job_throughput(world, T, t_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(inp["x"].nbytes + inp["logits"].nbytes),
                 "d2h_bytes_per_step": int(T * H * 4),

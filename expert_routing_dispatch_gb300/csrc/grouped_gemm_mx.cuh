@@ -20,9 +20,14 @@
 //
 // CTA = 10 warps: warp 0 issues the TMA loads of the E4M3 tiles into a 4-stage
 // ring; warp 1 owns TMEM (two 192-column accumulators and four 12-column scale
-// slots) and one of its threads issues the MMAs; warps 2..5 run the epilogue;
-// warps 6..9 (one per TMEM lane quadrant) gather each stage's scale words and
-// write them into the stage's scale slot with tcgen05.st.  Every wait is bounded.
+// slots) and one of its threads issues, per k-block, three tcgen05.cp of the
+// stage's scale words (shared memory -> TMEM, each 32 rows x 16 bytes copied to
+// all four lane quadrants) and the four MMAs, in order in the tensor pipe;
+// warps 2..5 run the epilogue; warps 6..9 gather the scale words from global
+// memory into the shared-memory chunks of ring slot warp - 6 (each warp owns one
+// slot and loads its next stage's words right after publishing one, so the
+// loads have four stages of MMAs to land before the warp's next proxy fence).
+// Every wait is bounded.
 #pragma once
 
 #include "common.cuh"
@@ -45,8 +50,30 @@ constexpr long long WAIT_LIMIT = 1ll << 31;
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
+#ifdef MOE_GEMM_PROFILE
+// Tuning builds only: clock cycles per role, summed over CTAs, per GEMM (gate/up, down).
+// [0] producer waits on a free stage [1] producer total [2] MMA waits on an accumulator
+// [3] MMA waits on loaded data [4] MMA waits on scale factors [5] MMA total
+// [6] epilogue waits (per warp) [7] epilogue total [8] scale warps wait on a free slot
+// [9] scale warps total [10] tiles [11] CTAs
+__device__ unsigned long long g_mx_prof[2][12];
+#define MX_PROF_WAIT(acc, call)                 \
+    ([&]() {                                    \
+        const long long _t = clock64();         \
+        const bool _r = (call);                 \
+        acc += clock64() - _t;                  \
+        return _r;                              \
+    }())
+#define MX_PROF_ADD(i, v) atomicAdd(&g_mx_prof[MODE][i], (unsigned long long)(v))
+#else
+#define MX_PROF_WAIT(acc, call) (call)
+#define MX_PROF_ADD(i, v) ((void)0)
+#endif
+
 struct Ctl {
     alignas(128) uint4 stage[4][32 * 8];  // down epilogue: 32-row x 128-byte fp32 staging per warp
+    // scale words per ring stage: [A | B columns 0-3 | B columns 4-5, 2 spare], each 32 rows x 16 bytes
+    alignas(128) uint4 sf[STAGES][3][32];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t sffull[STAGES];
@@ -105,15 +132,16 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
+// 32 rows x 16 bytes of shared memory (rows contiguous, no swizzle) -> lanes r of every
+// 32-lane quadrant, 4 columns from taddr
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;   // leading byte offset (one 16-byte column)
+    d |= (uint64_t)(128u >> 4) << 32;  // stride byte offset: 8-row groups of 16-byte rows
+    d |= (uint64_t)1 << 46;            // descriptor version; layout 0 = no swizzle
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
 }
-__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // UE8M0 code of a block whose largest magnitude is amax (OCP MX: floor(log2(amax))
 // - 8 + 127, clamped to [0, 254]; 0 for amax = 0 or below the normal range)
@@ -147,7 +175,7 @@ __device__ __forceinline__ void init(Ctl& c) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&c.full[s]), 1);
             mbar_init(smem_u32(&c.empty[s]), 1);
-            mbar_init(smem_u32(&c.sffull[s]), 4);
+            mbar_init(smem_u32(&c.sffull[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&c.tfull[a]), 1);
@@ -215,6 +243,9 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
+            long long w0 = 0, t0 = clock64();
+            (void)w0;
+            (void)t0;
             const uint64_t pol = l2_policy_evict_last();
             int g = 0;
             bool ok = true;
@@ -223,8 +254,8 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                 const int b_row = tc.e * args.w_rows + tc.nt * args.n_step;
                 for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
                     const int s = g % STAGES, r = g / STAGES;
-                    if (!mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag, args.status,
-                                           WAIT_LIMIT)) {
+                    if (!MX_PROF_WAIT(w0, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
+                                                            args.status, WAIT_LIMIT))) {
                         ok = false;
                         break;
                     }
@@ -239,28 +270,42 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                     }
                 }
             }
+            MX_PROF_ADD(0, w0);
+            MX_PROF_ADD(1, clock64() - t0);
+            MX_PROF_ADD(11, 1);
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
+            long long wa = 0, wf = 0, ws = 0, t0 = clock64();
+            (void)wa;
+            (void)wf;
+            (void)ws;
+            (void)t0;
             int g = 0, it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && !*abort_flag && next_tile(c, n, tile, e_hint, tc);
                  tile += gridDim.x, ++it) {
                 const int acc = it & 1, use = it >> 1;
-                if (!mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag, args.status, WAIT_LIMIT))
+                if (!MX_PROF_WAIT(wa, mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag,
+                                                        args.status, WAIT_LIMIT)))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * ACC_COLS);
                 for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
                     const int s = g % STAGES, r = g / STAGES;
-                    if (!mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status, WAIT_LIMIT) ||
-                        !mbar_wait_bounded(smem_u32(&c.sffull[s]), r & 1, abort_flag, args.status, WAIT_LIMIT)) {
+                    if (!MX_PROF_WAIT(wf, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status,
+                                                            WAIT_LIMIT)) ||
+                        !MX_PROF_WAIT(ws, mbar_wait_bounded(smem_u32(&c.sffull[s]), r & 1, abort_flag, args.status,
+                                                            WAIT_LIMIT))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sfa = c.tmem_base + (uint32_t)(SF_COL0 + s * SF_SLOT);
+                    tmem_cp_32x128b_x4(sfa, smem_u32(&c.sf[s][0][0]));
+                    tmem_cp_32x128b_x4(sfa + 4, smem_u32(&c.sf[s][1][0]));
+                    tmem_cp_32x128b_x4(sfa + 8, smem_u32(&c.sf[s][2][0]));
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         mma_mxf8(d_tmem, sdesc_k_swz<128>(a_addr(s) + j * 32), sdesc_k_swz<128>(b_addr(s) + j * 32),
@@ -270,60 +315,76 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                 if (!ok) break;
                 tc_commit(smem_u32(&c.tfull[acc]));
             }
+            MX_PROF_ADD(2, wa);
+            MX_PROF_ADD(3, wf);
+            MX_PROF_ADD(4, ws);
+            MX_PROF_ADD(5, clock64() - t0);
+            MX_PROF_ADD(10, it);
         }
     } else if (warp >= 6) {
-        // ================= scale-factor warps (lane quadrant q = warp % 4) =================
-        const int q = warp & 3;
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        // ================= scale-factor warps: warp 6 + j fills ring slot j =================
+        static_assert(STAGES == 4, "one scale warp per ring slot");
+        const int j = warp - 6;
         const long long b_total = (long long)n * args.w_rows;
-        int g = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; ok && !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
+        // stage g = k-block g % kblocks of this CTA's tile number g / kblocks; lane r = row r of each chunk
+        auto load = [&](int g, uint32_t (&w)[10]) -> bool {
+            const int kb = g % args.kblocks;
+            if (!next_tile(c, n, blockIdx.x + (g / args.kblocks) * (int)gridDim.x, e_hint, tc)) return false;
             const long long a_row = (long long)c.row_off[tc.e] + tc.mt * BM + lane;
             const long long b_row = (long long)tc.e * args.w_rows + tc.nt * args.n_step + lane;
-            for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
-                const int s = g % STAGES, r = g / STAGES;
-                uint32_t va[4], vb[6];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const long long row = a_row + 32 * i;
-                    va[i] = row < args.a_rows ? __ldg(args.a_s + row * args.kblocks + kb) : 0u;
-                }
-#pragma unroll
-                for (int i = 0; i < 6; ++i) {
-                    long long row;
-                    const uint32_t* src;
-                    if (MODE == MODE_GATEUP) {  // columns 0-2: gate rows, 3-5: up rows of the same h columns
-                        row = b_row + 32 * (i % 3);
-                        src = i < 3 ? args.b0_s : args.b1_s;
-                    } else {
-                        row = b_row + 32 * i;
-                        src = args.b0_s;
-                    }
-                    vb[i] = row < b_total ? __ldg(src + row * args.kblocks + kb) : 0u;
-                }
-                if (!mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag, args.status, WAIT_LIMIT)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t slot = c.tmem_base + lane_off + (uint32_t)(SF_COL0 + s * SF_SLOT);
-                tmem_st4(slot, va[0], va[1], va[2], va[3]);
-                tmem_st4(slot + 4, vb[0], vb[1], vb[2], vb[3]);
-                tmem_st2(slot + 8, vb[4], vb[5]);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&c.sffull[s]));
+            for (int i = 0; i < 4; ++i) {
+                const long long row = a_row + 32 * i;
+                w[i] = row < args.a_rows ? __ldg(args.a_s + row * args.kblocks + kb) : 0u;
             }
+#pragma unroll
+            for (int i = 0; i < 6; ++i) {
+                long long row;
+                const uint32_t* src;
+                if (MODE == MODE_GATEUP) {  // columns 0-2: gate rows, 3-5: up rows of the same h columns
+                    row = b_row + 32 * (i % 3);
+                    src = i < 3 ? args.b0_s : args.b1_s;
+                } else {
+                    row = b_row + 32 * i;
+                    src = args.b0_s;
+                }
+                w[4 + i] = row < b_total ? __ldg(src + row * args.kblocks + kb) : 0u;
+            }
+            return true;
+        };
+        long long wsf = 0, tsf = clock64();
+        (void)wsf;
+        (void)tsf;
+        uint32_t w[10];
+        for (int g = j; load(g, w) && !*abort_flag; g += STAGES) {
+            const int r = g / STAGES;
+            // the copies of this slot's previous round have completed with its MMAs
+            if (!MX_PROF_WAIT(wsf, mbar_wait_bounded(smem_u32(&c.empty[j]), (r & 1) ^ 1, abort_flag, args.status,
+                                                     WAIT_LIMIT)))
+                break;
+            c.sf[j][0][lane] = make_uint4(w[0], w[1], w[2], w[3]);
+            c.sf[j][1][lane] = make_uint4(w[4], w[5], w[6], w[7]);
+            c.sf[j][2][lane] = make_uint4(w[8], w[9], 0u, 0u);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by tcgen05.cp (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&c.sffull[j]));
+        }
+        if (lane == 0) {
+            MX_PROF_ADD(8, wsf);
+            MX_PROF_ADD(9, clock64() - tsf);
         }
     } else {
         // ================= epilogue (warps 2..5, TMEM lane quarter q = warp % 4) =================
         const int q = warp & 3;
+        long long wt = 0, t0 = clock64();
+        (void)wt;
+        (void)t0;
         int it = 0;
         for (int tile = blockIdx.x; !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++it) {
             const int acc = it & 1, use = it >> 1;
-            if (!mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status, WAIT_LIMIT)) break;
+            if (!MX_PROF_WAIT(wt, mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status,
+                                                    WAIT_LIMIT)))
+                break;
             tc_fence_after();
             const int row0_in_e = tc.mt * BM + q * 32;
             const long long grow0 = (long long)c.row_off[tc.e] + row0_in_e;
@@ -395,6 +456,10 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
         }
         // the h codes are read later through TMA (async proxy)
         asm volatile("fence.proxy.async.global;" ::: "memory");
+        if (lane == 0) {
+            MX_PROF_ADD(6, wt);
+            MX_PROF_ADD(7, clock64() - t0);
+        }
     }
 }
 

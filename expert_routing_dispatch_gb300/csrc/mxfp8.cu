@@ -200,3 +200,15 @@ cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int
 }
 
 }  // namespace moe
+
+#ifdef MOE_GEMM_PROFILE
+// tuning builds only: read (and optionally reset) the role counters of grouped_gemm_mx.cuh
+extern "C" int moe_debug_mx_prof(unsigned long long* host24, int reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(host24, moe::mx::g_mx_prof, sizeof(unsigned long long) * 24);
+    if (reset) {
+        unsigned long long z[24] = {};
+        e = cudaMemcpyToSymbol(moe::mx::g_mx_prof, z, sizeof(z));
+    }
+    return e == cudaSuccess ? 0 : 4;
+}
+#endif
