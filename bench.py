@@ -36,6 +36,7 @@ L2_FLUSH_BYTES = 256 << 20
 _CS = "expert_routing_dispatch_gb300/csrc/"
 KERNEL_SOURCES = {
     "grouped_gemm_gate_up": [_CS + "grouped_ffn.cu", _CS + "grouped_gemm.cuh", _CS + "common.cuh"],
+    "grouped_ffn_mx": [_CS + "mxfp8.cu", _CS + "grouped_gemm_mx.cuh", _CS + "common.cuh"],
     "moe_layer_fused": [_CS + "decode_fused.cu", _CS + "grouped_gemm.cuh", _CS + "common.cuh", _CS + "route.cuh",
                         _CS + "combine.cuh"],
 }
