@@ -86,3 +86,25 @@ def test_missing_workspace_rejected(moe):
     assert L.moe_dispatch(ctypes.byref(d), ok, ok, ok, ok, ok, ok, ok, None, nd, None) == 3
     nf = moe.moe_expert_ffn_workspace_size(d)
     assert L.moe_expert_ffn(ctypes.byref(d), ok, ok, ok, ok, ok, ok, ok, nf - 256, None, None) == 3
+
+
+def test_mxfp8_entries_reject_bad_arguments_without_gpu(moe):
+    L = moe.lib()
+    ok = 1 << 20
+    # H or I not a multiple of 128: unsupported by the MXFP8 entries (fine for the bf16 ones)
+    for dims in ((64, 192, 128, 8, 2, 0, 8), (64, 256, 192, 8, 2, 0, 8)):
+        d = moe.Dims(*dims)
+        assert moe.moe_workspace_size(d) > 0
+        assert moe.moe_layer_mxfp8_workspace_size(d) == 0 and moe.moe_expert_ffn_mxfp8_workspace_size(d) == 0
+        assert L.moe_layer_mxfp8(ctypes.byref(d), *([ok] * 9), None, None, ok, 1 << 40, None, None) == 2
+        assert L.moe_expert_ffn_mxfp8(ctypes.byref(d), *([ok] * 10), ok, 1 << 40, None, None) == 2
+    d = moe.Dims(64, 256, 128, 16, 4, 0, 16)
+    need = moe.moe_layer_mxfp8_workspace_size(d)
+    assert need > moe.moe_expert_ffn_mxfp8_workspace_size(d) > 0
+    assert L.moe_layer_mxfp8(ctypes.byref(d), *([ok] * 9), None, None, ok, need - 1, None, None) == 3
+    assert L.moe_layer_mxfp8(ctypes.byref(d), ok + 4, *([ok] * 8), None, None, ok, need, None, None) == 1
+    # quantiser: K a positive multiple of 32, aligned pointers
+    assert L.moe_quantize_mxfp8(ok, 4, 48, ok, ok, None) == 1
+    assert L.moe_quantize_mxfp8(ok, -1, 64, ok, ok, None) == 1
+    assert L.moe_quantize_mxfp8(ok + 2, 4, 64, ok, ok, None) == 1
+    assert L.moe_quantize_mxfp8(ok, 0, 64, ok, ok, None) == 0  # nothing to do, no launch

@@ -193,3 +193,59 @@ def test_mx_layer(moe, name):
     print(f"PARITY mxfp8 layer {name} max|gpu-oracle_mx|/RMS = {err / rms:.3e} (vs the bf16 oracle: "
           f"{e16 / rms16:.3e})")
     assert err <= 2e-2 * rms
+
+
+@pytest.mark.parametrize("dims", [
+    (1, 128, 128, 4, 1, 0, 4),        # T = 1, k = 1
+    (300, 384, 640, 8, 2, 1, 5),      # I = 6.67 gate/up tiles of 96 columns, H = 2 down tiles of 192
+    (513, 256, 128, 3, 1, 1, 2),      # one local expert, m-tile tail, I smaller than a gate/up tile
+    (37, 128, 256, 8, 8, 2, 5),       # k = E, partial range
+])
+def test_mx_layer_small_shapes(moe, dims):
+    import torch
+
+    T, H, I, E, k, e0, e1 = dims
+    n = e1 - e0
+    x = synth.normal_bf16(0, synth.TID_X, (T, H), 1.0)
+    lg = synth.normal_f32(0, synth.TID_LOGITS, (T, E))
+    wb = {key: synth.normal_bf16(0, tid, shape, 0.05, start=e0 * shape[1] * shape[2])
+          for key, tid, shape in (("w_gate", synth.TID_W_GATE, (n, I, H)), ("w_up", synth.TID_W_UP, (n, I, H)),
+                                  ("w_down", synth.TID_W_DOWN, (n, H, I)))}
+    w = {}
+    for key, a in wb.items():
+        q, s = oracle.mxfp8_quantize(a.reshape(-1, a.shape[-1]))
+        w[key] = (q.reshape(a.shape), s.reshape(a.shape[:-1] + (a.shape[-1] // 32,)))
+    dw = {key: (dev(q), dev(s)) for key, (q, s) in w.items()}
+    dims_ = moe.Dims(*dims)
+    out = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    idx = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = moe.alloc_workspace(moe.moe_layer_mxfp8_workspace_size(dims_))
+    moe.moe_layer_mxfp8(dims_, dev(x), dev(lg), dw["w_gate"], dw["w_up"], dw["w_down"], out, ws, topk_idx=idx,
+                        topk_w=wt, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    st, ridx, rw = oracle.route(lg, k)
+    assert np.array_equal(host(idx), ridx)
+    d = oracle.dispatch(ridx, e0, e1)
+    P, R = T * k, d["R"]
+    xq_t, xs_t = oracle.mxfp8_quantize(x)
+    xq = np.zeros((P, H), np.uint8)
+    xs = np.zeros((P, H // 32), np.uint8)
+    xq[:R] = xq_t[d["row_pair"] // k]
+    xs[:R] = xs_t[d["row_pair"] // k]
+    y_perm = np.zeros((P, H), np.float32)
+    if R:
+        rows = np.arange(R, dtype=np.int64)
+        y_perm[:R] = oracle.expert_ffn_mxfp8_rowlist(xq, xs, d["offsets"], w["w_gate"], w["w_up"], w["w_down"],
+                                                     rows).astype(np.float32)
+    ref = oracle.combine_tokens(y_perm, d["pair_row"], rw.astype(np.float32))
+    got = host(out)
+    if R == 0:
+        assert (got == 0).all()
+        return
+    err, rms = rel_err(got, ref)
+    print(f"PARITY mxfp8 small {dims} max|gpu-oracle_mx|/RMS = {err / rms:.3e}")
+    assert err <= 2e-2 * rms
+
