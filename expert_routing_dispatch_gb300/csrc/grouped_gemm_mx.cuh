@@ -53,7 +53,7 @@ enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 #ifdef MOE_GEMM_PROFILE
 // Tuning builds only: clock cycles per role, summed over CTAs, per GEMM (gate/up, down).
 // [0] producer waits on a free stage [1] producer total [2] MMA waits on an accumulator
-// [3] MMA waits on loaded data [4] MMA waits on scale factors [5] MMA total
+// [3] MMA waits on a stage (data and scales) [4] unused [5] MMA total
 // [6] epilogue waits (per warp) [7] epilogue total [8] scale warps wait on a free slot
 // [9] scale warps total [10] tiles [11] CTAs
 __device__ unsigned long long g_mx_prof[2][12];
@@ -74,9 +74,8 @@ struct Ctl {
     alignas(128) uint4 stage[4][32 * 8];  // down epilogue: 32-row x 128-byte fp32 staging per warp
     // scale words per ring stage: [A | B columns 0-3 | B columns 4-5, 2 spare], each 32 rows x 16 bytes
     alignas(128) uint4 sf[STAGES][3][32];
-    uint64_t full[STAGES];
+    uint64_t full[STAGES];  // the stage's TMA bytes (producer's expect-tx arrival) and its scale chunk (scale warp)
     uint64_t empty[STAGES];
-    uint64_t sffull[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -173,9 +172,8 @@ __device__ __forceinline__ void init(Ctl& c) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&c.full[s]), 1);
+            mbar_init(smem_u32(&c.full[s]), 2);
             mbar_init(smem_u32(&c.empty[s]), 1);
-            mbar_init(smem_u32(&c.sffull[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&c.tfull[a]), 1);
@@ -277,10 +275,9 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            long long wa = 0, wf = 0, ws = 0, t0 = clock64();
+            long long wa = 0, wf = 0, t0 = clock64();
             (void)wa;
             (void)wf;
-            (void)ws;
             (void)t0;
             int g = 0, it = 0;
             bool ok = true;
@@ -295,8 +292,6 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                 for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
                     const int s = g % STAGES, r = g / STAGES;
                     if (!MX_PROF_WAIT(wf, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status,
-                                                            WAIT_LIMIT)) ||
-                        !MX_PROF_WAIT(ws, mbar_wait_bounded(smem_u32(&c.sffull[s]), r & 1, abort_flag, args.status,
                                                             WAIT_LIMIT))) {
                         ok = false;
                         break;
@@ -317,7 +312,6 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
             }
             MX_PROF_ADD(2, wa);
             MX_PROF_ADD(3, wf);
-            MX_PROF_ADD(4, ws);
             MX_PROF_ADD(5, clock64() - t0);
             MX_PROF_ADD(10, it);
         }
@@ -367,7 +361,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
             c.sf[j][2][lane] = make_uint4(w[8], w[9], 0u, 0u);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by tcgen05.cp (async proxy)
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&c.sffull[j]));
+            if (lane == 0) mbar_arrive(smem_u32(&c.full[j]));
         }
         if (lane == 0) {
             MX_PROF_ADD(8, wsf);
