@@ -142,6 +142,20 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// true in exactly one lane of the (converged) warp: the lowest active lane.  An
+// issuing warp keeps all 32 lanes in its loop and issues its tcgen05 operations
+// (and the commits that track them) under elect_one(), so they all come from the
+// same lane; a single lane looping alone while the other 31 wait at the CTA
+// barrier issues them markedly slower.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(p)::"memory");
+    return p != 0;
+}
 // mbarrier arrive once all previously issued tcgen05 ops of this thread completed
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -19,8 +19,8 @@
 //
 // CTA = 6 warps: warp 0 issues TMA loads (128-byte swizzle) into a 4-stage
 // shared-memory ring; warp 1 owns 512 TMEM columns (two 256-column fp32
-// accumulators) and one of its threads issues tcgen05.mma (M=128, N=256,
-// K=16); warps 2..5 drain TMEM with tcgen05.ld and run the epilogue while the
+// accumulators) and issues tcgen05.mma (M=128, N=256, K=16) from one elected
+// lane while all 32 lanes run the loop; warps 2..5 drain TMEM with tcgen05.ld and run the epilogue while the
 // next tile accumulates into the other buffer.  Every wait is bounded: on
 // timeout the status word gets MOE_ERR_TIMEOUT and all roles bail out.
 #pragma once
@@ -234,8 +234,8 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
     auto b_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES + A_BYTES); };
 
     if (warp == 0) {
-        // ================= TMA producer =================
-        if (lane == 0) {
+        // ================= TMA producer: the whole warp loops, the elected lane issues =================
+        {
             long long w_empty = 0, t_begin = clock64();
             (void)w_empty;
             (void)t_begin;
@@ -255,7 +255,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
 #endif
             int e_hint = 0;
             TileCoord tc;
-            bool ok = !*abort_flag;
+            bool ok = !__any_sync(0xffffffffu, *abort_flag);
             for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
                 const int a_row = c.row_off[tc.e] + tc.mt * BM;
                 const int piece_rows = args.n_step >> tc.shift;  // weight rows of one map's box
@@ -268,39 +268,46 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                 const uint32_t stage_tx = (uint32_t)((a_small ? args.a_small : BM) * BK * 2 + bn_t * BK * 2);
                 for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                     const int s = p.g % STAGES, r = p.g / STAGES;
-                    if (!MOE_PROF_WAIT(w_empty, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
-                                                                  args.status, WAIT_LIMIT))) {
+                    if (!__all_sync(0xffffffffu,
+                                    MOE_PROF_WAIT(w_empty, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1,
+                                                                             abort_flag, args.status, WAIT_LIMIT)))) {
                         ok = false;
                         break;
                     }
-                    // The first m-tile of each weight tile pulls the weight boxes PF k-blocks
-                    // ahead into L2 (only boxes wholly inside the tensor).
-                    const int PF = args.prefetch;
-                    if (PF > 0 && tc.shift == 0 && tc.mt == 0 && kb + PF < args.kblocks &&
-                        b_row + (MODE == MODE_GATEUP ? args.bn / 2 : args.bn) <= n * args.b_rows) {
-                        tma_prefetch_l2_2d(tmB0, (kb + PF) * BK, b_row);
-                        if (MODE == MODE_GATEUP) tma_prefetch_l2_2d(tmB1, (kb + PF) * BK, b_row);
-                    }
-                    const uint32_t fb = smem_u32(&c.full[s]);
-                    mbar_arrive_expect_tx(fb, stage_tx);
                     p.issued[s] = r + 1;
-                    tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
-                    if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn_t/2 each
-                        tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
-                        tma_load_2d(b_addr(s) + (uint32_t)(bn_t / 2) * BK * 2, tmB1, kb * BK, b_row, fb, pol_b);
-                    } else {
-                        tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
+                    if (elect_one()) {
+                        // The first m-tile of each weight tile pulls the weight boxes PF k-blocks
+                        // ahead into L2 (only boxes wholly inside the tensor).
+                        const int PF = args.prefetch;
+                        if (PF > 0 && tc.shift == 0 && tc.mt == 0 && kb + PF < args.kblocks &&
+                            b_row + (MODE == MODE_GATEUP ? args.bn / 2 : args.bn) <= n * args.b_rows) {
+                            tma_prefetch_l2_2d(tmB0, (kb + PF) * BK, b_row);
+                            if (MODE == MODE_GATEUP) tma_prefetch_l2_2d(tmB1, (kb + PF) * BK, b_row);
+                        }
+                        const uint32_t fb = smem_u32(&c.full[s]);
+                        mbar_arrive_expect_tx(fb, stage_tx);
+                        tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
+                        if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn_t/2 each
+                            tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
+                            tma_load_2d(b_addr(s) + (uint32_t)(bn_t / 2) * BK * 2, tmB1, kb * BK, b_row, fb, pol_b);
+                        } else {
+                            tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
+                        }
                     }
+                    __syncwarp();
                 }
             }
 #ifdef MOE_GEMM_PROFILE
-            atomicAdd(&g_gemm_prof[0], (unsigned long long)w_empty);
-            atomicAdd(&g_gemm_prof[1], (unsigned long long)(clock64() - t_begin));
+            if (lane == 0) {
+                atomicAdd(&g_gemm_prof[0], (unsigned long long)w_empty);
+                atomicAdd(&g_gemm_prof[1], (unsigned long long)(clock64() - t_begin));
+            }
 #endif
         }
     } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
+        // ================= MMA issuer: the whole warp loops, the elected lane issues =================
+        // (every branch is warp-uniform, so elect_one() always picks the same lane)
+        {
             long long w_acc = 0, w_full = 0, t_begin = clock64(), ntiles = 0;
             (void)w_acc;
             (void)w_full;
@@ -308,40 +315,49 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             (void)ntiles;
             int e_hint = 0;
             TileCoord tc;
-            bool ok = !*abort_flag;
+            bool ok = !__any_sync(0xffffffffu, *abort_flag);
+            const uint64_t a_desc0 = sdesc_k_swz<ROW_BYTES>(a_addr(0)), b_desc0 = sdesc_k_swz<ROW_BYTES>(b_addr(0));
             for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++p.it) {
                 const int acc = p.it & 1, use = p.it >> 1;
                 ++ntiles;
-                if (!MOE_PROF_WAIT(w_acc, mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag,
-                                                            args.status, WAIT_LIMIT)))
+                if (!__all_sync(0xffffffffu, MOE_PROF_WAIT(w_acc, mbar_wait_bounded(smem_u32(&c.tempty[acc]),
+                                                                                   (use & 1) ^ 1, abort_flag,
+                                                                                   args.status, WAIT_LIMIT))))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * BN);
                 const uint32_t idesc = idesc_bf16_f32(BM, args.bn >> tc.shift);
                 for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                     const int s = p.g % STAGES, r = p.g / STAGES;
-                    if (!MOE_PROF_WAIT(w_full, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status,
-                                                                 WAIT_LIMIT))) {
+                    if (!__all_sync(0xffffffffu, MOE_PROF_WAIT(w_full, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1,
+                                                                                       abort_flag, args.status,
+                                                                                       WAIT_LIMIT)))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    if (elect_one()) {
+                        // descriptors are linear in the address (bits 0-13 hold address >> 4)
+                        const uint64_t ad = a_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
+                        const uint64_t bd = b_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = sdesc_k_swz<ROW_BYTES>(a_addr(s) + kk * 32);
-                        const uint64_t bd = sdesc_k_swz<ROW_BYTES>(b_addr(s) + kk * 32);
-                        tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
+                            tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                        tc_commit(smem_u32(&c.empty[s]));
                     }
-                    tc_commit(smem_u32(&c.empty[s]));
+                    __syncwarp();
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&c.tfull[acc]));
+                if (elect_one()) tc_commit(smem_u32(&c.tfull[acc]));
+                __syncwarp();
             }
 #ifdef MOE_GEMM_PROFILE
-            atomicAdd(&g_gemm_prof[2], (unsigned long long)w_acc);
-            atomicAdd(&g_gemm_prof[3], (unsigned long long)w_full);
-            atomicAdd(&g_gemm_prof[4], (unsigned long long)(clock64() - t_begin));
-            atomicAdd(&g_gemm_prof[7], (unsigned long long)ntiles);
+            if (lane == 0) {
+                atomicAdd(&g_gemm_prof[2], (unsigned long long)w_acc);
+                atomicAdd(&g_gemm_prof[3], (unsigned long long)w_full);
+                atomicAdd(&g_gemm_prof[4], (unsigned long long)(clock64() - t_begin));
+                atomicAdd(&g_gemm_prof[7], (unsigned long long)ntiles);
+            }
 #endif
         }
     } else {
@@ -456,8 +472,10 @@ __device__ __forceinline__ void teardown(Ctl& c, Pipe& p, int32_t* status) {
             }
     }
     if (warp == 1) {
+        // the lane that issued the MMAs (elect_one() of the converged warp) commits the drain
+        if (elect_one()) tc_commit(smem_u32(&c.drain));
+        __syncwarp();
         if (lane == 0) {
-            tc_commit(smem_u32(&c.drain));
             volatile int never = 0;
             mbar_wait_bounded(smem_u32(&c.drain), 0, &never, status, WAIT_LIMIT);
         }

@@ -239,24 +239,25 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
     TileCoord tc;
 
     if (warp == 0) {
-        // ================= TMA producer =================
-        if (lane == 0) {
-            long long w0 = 0, t0 = clock64();
-            (void)w0;
-            (void)t0;
-            const uint64_t pol = l2_policy_evict_last();
-            int g = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
-                const int a_row = c.row_off[tc.e] + tc.mt * BM;
-                const int b_row = tc.e * args.w_rows + tc.nt * args.n_step;
-                for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
-                    const int s = g % STAGES, r = g / STAGES;
-                    if (!MX_PROF_WAIT(w0, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
-                                                            args.status, WAIT_LIMIT))) {
-                        ok = false;
-                        break;
-                    }
+        // ================= TMA producer: the whole warp loops, the elected lane issues =================
+        long long w0 = 0, t0 = clock64();
+        (void)w0;
+        (void)t0;
+        const uint64_t pol = l2_policy_evict_last();
+        int g = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile(c, n, tile, e_hint, tc);
+             tile += gridDim.x) {
+            const int a_row = c.row_off[tc.e] + tc.mt * BM;
+            const int b_row = tc.e * args.w_rows + tc.nt * args.n_step;
+            for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
+                const int s = g % STAGES, r = g / STAGES;
+                if (!__all_sync(0xffffffffu, MX_PROF_WAIT(w0, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1,
+                                                                               abort_flag, args.status, WAIT_LIMIT)))) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
                     const uint32_t fb = smem_u32(&c.full[s]);
                     mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
                     tma_load_2d(a_addr(s), tmA, kb * BKB, a_row, fb, pol);
@@ -267,49 +268,63 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                         tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
                     }
                 }
+                __syncwarp();
             }
+        }
+        if (lane == 0) {
             MX_PROF_ADD(0, w0);
             MX_PROF_ADD(1, clock64() - t0);
             MX_PROF_ADD(11, 1);
         }
     } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
-            long long wa = 0, wf = 0, t0 = clock64();
-            (void)wa;
-            (void)wf;
-            (void)t0;
-            int g = 0, it = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && !*abort_flag && next_tile(c, n, tile, e_hint, tc);
-                 tile += gridDim.x, ++it) {
-                const int acc = it & 1, use = it >> 1;
-                if (!MX_PROF_WAIT(wa, mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag,
-                                                        args.status, WAIT_LIMIT)))
+        // ================= MMA issuer: the whole warp loops, the elected lane issues =================
+        // Every branch below is warp-uniform (waits and the abort flag are combined over the
+        // warp), so elect_one() always sees 32 lanes and picks the same one.
+        long long wa = 0, wf = 0, t0 = clock64();
+        (void)wa;
+        (void)wf;
+        (void)t0;
+        int g = 0, it = 0;
+        bool ok = true;
+        const uint32_t sf_smem = smem_u32(&c.sf[0][0][0]);
+        const uint64_t a_desc0 = sdesc_k_swz<128>(a_addr(0)), b_desc0 = sdesc_k_swz<128>(b_addr(0));
+        for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile(c, n, tile, e_hint, tc);
+             tile += gridDim.x, ++it) {
+            const int acc = it & 1, use = it >> 1;
+            if (!__all_sync(0xffffffffu, MX_PROF_WAIT(wa, mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1,
+                                                                           abort_flag, args.status, WAIT_LIMIT))))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * ACC_COLS);
+            for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
+                const int s = g % STAGES, r = g / STAGES;
+                if (!__all_sync(0xffffffffu, MX_PROF_WAIT(wf, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1,
+                                                                               abort_flag, args.status, WAIT_LIMIT)))) {
+                    ok = false;
                     break;
+                }
                 tc_fence_after();
-                const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * ACC_COLS);
-                for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
-                    const int s = g % STAGES, r = g / STAGES;
-                    if (!MX_PROF_WAIT(wf, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status,
-                                                            WAIT_LIMIT))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                if (elect_one()) {
                     const uint32_t sfa = c.tmem_base + (uint32_t)(SF_COL0 + s * SF_SLOT);
-                    tmem_cp_32x128b_x4(sfa, smem_u32(&c.sf[s][0][0]));
-                    tmem_cp_32x128b_x4(sfa + 4, smem_u32(&c.sf[s][1][0]));
-                    tmem_cp_32x128b_x4(sfa + 8, smem_u32(&c.sf[s][2][0]));
+                    const uint32_t sfs = sf_smem + (uint32_t)(s * 3 * 32 * 16);
+                    tmem_cp_32x128b_x4(sfa, sfs);
+                    tmem_cp_32x128b_x4(sfa + 4, sfs + 32 * 16);
+                    tmem_cp_32x128b_x4(sfa + 8, sfs + 2 * 32 * 16);
+                    // descriptors are linear in the address (bits 0-13 hold address >> 4)
+                    const uint64_t ad = a_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
+                    const uint64_t bd = b_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        mma_mxf8(d_tmem, sdesc_k_swz<128>(a_addr(s) + j * 32), sdesc_k_swz<128>(b_addr(s) + j * 32),
-                                 idesc_mxf8(BM, BN, j), sfa, sfa + 4, (kb | j) != 0);
+                        mma_mxf8(d_tmem, ad + 2 * j, bd + 2 * j, idesc_mxf8(BM, BN, j), sfa, sfa + 4, (kb | j) != 0);
                     tc_commit(smem_u32(&c.empty[s]));
                 }
-                if (!ok) break;
-                tc_commit(smem_u32(&c.tfull[acc]));
+                __syncwarp();
             }
+            if (!ok) break;
+            if (elect_one()) tc_commit(smem_u32(&c.tfull[acc]));
+            __syncwarp();
+        }
+        if (lane == 0) {
             MX_PROF_ADD(2, wa);
             MX_PROF_ADD(3, wf);
             MX_PROF_ADD(5, clock64() - t0);
@@ -463,8 +478,10 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
 __device__ __forceinline__ void teardown(Ctl& c, int32_t* status) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 1) {
+        // the lane that issued the MMAs (elect_one() of the converged warp) commits the drain
+        if (elect_one()) tc_commit(smem_u32(&c.drain));
+        __syncwarp();
         if (lane == 0) {
-            tc_commit(smem_u32(&c.drain));
             volatile int never = 0;
             mbar_wait_bounded(smem_u32(&c.drain), 0, &never, status, WAIT_LIMIT);
             if (c.abort_flag) {  // copies may still be in flight: let them land
