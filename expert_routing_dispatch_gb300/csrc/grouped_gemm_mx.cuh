@@ -258,13 +258,15 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                     break;
                 }
                 if (elect_one()) {
+                    // gate/up: weight boxes before the token box; down: token box first
                     const uint32_t fb = smem_u32(&c.full[s]);
                     mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
-                    tma_load_2d(a_addr(s), tmA, kb * BKB, a_row, fb, pol);
                     if (MODE == MODE_GATEUP) {  // [96 gate rows | 96 up rows]
                         tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
                         tma_load_2d(b_addr(s) + (uint32_t)(BN / 2) * BKB, tmB1, kb * BKB, b_row, fb, pol);
+                        tma_load_2d(a_addr(s), tmA, kb * BKB, a_row, fb, pol);
                     } else {
+                        tma_load_2d(a_addr(s), tmA, kb * BKB, a_row, fb, pol);
                         tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
                     }
                 }
