@@ -156,6 +156,11 @@ __device__ __forceinline__ bool elect_one() {
         : "=r"(p)::"memory");
     return p != 0;
 }
+// SiLU(a) = a / (1 + e^-a) with the fast reciprocal-multiply divide: the gate/up
+// epilogue warp shares its SM sub-partition with an issuing warp, so its instruction
+// count matters.  For a < -88 the denominator is +inf and the result 0 (exact SiLU
+// there is below 1e-36).
+__device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.f + __expf(-a)); }
 // mbarrier arrive once all previously issued tcgen05 ops of this thread completed
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

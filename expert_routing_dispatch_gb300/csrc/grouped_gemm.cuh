@@ -401,10 +401,10 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     for (int i = 0; i < 8; ++i) {
                         const float a0 = __uint_as_float(g0[2 * i]), a1 = __uint_as_float(g0[2 * i + 1]);
                         const float b0 = __uint_as_float(u0[2 * i]), b1 = __uint_as_float(u0[2 * i + 1]);
-                        pk[i] = pack_bf16x2(a0 / (1.f + __expf(-a0)) * b0, a1 / (1.f + __expf(-a1)) * b1);
+                        pk[i] = pack_bf16x2(silu(a0) * b0, silu(a1) * b1);
                         const float c0 = __uint_as_float(g1[2 * i]), c1 = __uint_as_float(g1[2 * i + 1]);
                         const float d0 = __uint_as_float(u1[2 * i]), d1 = __uint_as_float(u1[2 * i + 1]);
-                        pk[8 + i] = pack_bf16x2(c0 / (1.f + __expf(-c0)) * d0, c1 / (1.f + __expf(-c1)) * d1);
+                        pk[8 + i] = pack_bf16x2(silu(c0) * d0, silu(c1) * d1);
                     }
                     const int sw = (lane >> 1) & 3;
 #pragma unroll

@@ -289,6 +289,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
         int g = 0, it = 0;
         bool ok = true;
         const uint32_t sf_smem = smem_u32(&c.sf[0][0][0]);
+        const uint32_t tmem = c.tmem_base;  // a register copy: the asm memory clobbers would reload it
         const uint64_t a_desc0 = sdesc_k_swz<128>(a_addr(0)), b_desc0 = sdesc_k_swz<128>(b_addr(0));
         for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile(c, n, tile, e_hint, tc);
              tile += gridDim.x, ++it) {
@@ -297,7 +298,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                                                                            abort_flag, args.status, WAIT_LIMIT))))
                 break;
             tc_fence_after();
-            const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * ACC_COLS);
+            const uint32_t d_tmem = tmem + (uint32_t)(acc * ACC_COLS);
             for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
                 const int s = g % STAGES, r = g / STAGES;
                 if (!__all_sync(0xffffffffu, MX_PROF_WAIT(wf, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1,
@@ -307,7 +308,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                 }
                 tc_fence_after();
                 if (elect_one()) {
-                    const uint32_t sfa = c.tmem_base + (uint32_t)(SF_COL0 + s * SF_SLOT);
+                    const uint32_t sfa = tmem + (uint32_t)(SF_COL0 + s * SF_SLOT);
                     const uint32_t sfs = sf_smem + (uint32_t)(s * 3 * 32 * 16);
                     tmem_cp_32x128b_x4(sfa, sfs);
                     tmem_cp_32x128b_x4(sfa + 4, sfs + 32 * 16);
@@ -419,8 +420,8 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                     for (int i = 0; i < 16; ++i) {
                         const float a0 = __uint_as_float(g0[i]), b0 = __uint_as_float(u0[i]);
                         const float a1 = __uint_as_float(g1[i]), b1 = __uint_as_float(u1[i]);
-                        h[i] = a0 / (1.f + __expf(-a0)) * b0;
-                        h[16 + i] = a1 / (1.f + __expf(-a1)) * b1;
+                        h[i] = silu(a0) * b0;
+                        h[16 + i] = silu(a1) * b1;
                     }
                     uint32_t w[8];
                     const uint32_t code = mx_quantize32(h, w);
