@@ -80,6 +80,26 @@ def job_throughput(world, tokens_per_rank, t_max_ms):
     return world * tokens_per_rank / (t_max_ms * 1e-3)
 
 
+def memory_bound_rates(T, E, k, H, R, t_local, kern_ms, hbm_gbs):
+    """Algorithmic GB/s of the HBM-bound entries of the split path, from the entry-by-entry
+    times (ms): routing reads the logits and writes k ids and weights per token; dispatch
+    reads the topk ids (histogram and placement passes), the x rows of the tokens with a
+    local slot, and writes the grouped rows with their indices; combine reads the fp32
+    y_perm rows, the slot rows and weights, and writes the fp32 output rows."""
+    b = {
+        "route": T * E * 4 + T * k * 8,
+        "dispatch": 2 * T * k * 4 + t_local * H * 2 + R * H * 2 + R * 4 + T * k * 4,
+        "combine": R * H * 4 + T * k * 8 + T * H * 4,
+    }
+    out = {}
+    for nm, by in b.items():
+        ms = kern_ms.get(nm)
+        if ms:
+            gbs = by / (ms * 1e-3) / 1e9
+            out[nm] = {"bytes": int(by), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_gbs, 4)}
+    return out
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -402,6 +422,7 @@ def run_ours(args):
     # routed rows and active local experts, counted from this run's routing
     ti = topk_idx.flatten()
     loc = ti[(ti >= e0) & (ti < e1)]
+    t_local = int(((topk_idx.view(T, k) >= e0) & (topk_idx.view(T, k) < e1)).any(dim=1).sum().item())
     R = int(loc.numel())
     active = int(torch.unique(loc).numel())
     t_step_max = reduce_max(t_step, world, dev)
@@ -544,6 +565,8 @@ def run_ours(args):
             "active_local_experts": active,
             "routed_rows_per_s": R / (t_step * 1e-3),
             "weight_gbs": weight_bytes / (t_step * 1e-3) / 1e9,
+            "memory_bound_entries": memory_bound_rates(T, E, k, H, int(loc.numel()), t_local, kern_ms,
+                                                        peaks["hbm_gbs"]) if not fused and not mx else {},
             "wall_s_timed_loop_incl_flush": round(wall, 4),
             "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
         },

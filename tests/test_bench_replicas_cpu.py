@@ -61,3 +61,22 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_memory_bound_rates_prefill_ep_rank_numbers():
+    """The GB/s the JSON line reports for the HBM-bound entries: bytes counted per the
+    stated formulas, rates from the entry times, fractions of the given HBM peak."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    T, E, k, H, R, t_local = 6000, 128, 8, 4096, 12014, 5000
+    r = bench.memory_bound_rates(T, E, k, H, R, t_local, {"route": 0.01, "combine": 0.0512}, 6796.9)
+    assert set(r) == {"route", "combine"}  # no time for dispatch -> not reported
+    assert r["route"]["bytes"] == 6000 * 128 * 4 + 6000 * 8 * 8 == 3_456_000
+    assert abs(r["route"]["gbs"] - 345.6) < 0.05
+    comb = 12014 * 4096 * 4 + 6000 * 8 * 8 + 6000 * 4096 * 4
+    assert r["combine"]["bytes"] == comb == 295_525_376
+    assert abs(r["combine"]["gbs"] - comb / 0.0512e-3 / 1e9) < 0.05
+    assert abs(r["combine"]["frac_of_hbm"] - r["combine"]["gbs"] / 6796.9) < 1e-4
+    d = bench.memory_bound_rates(T, E, k, H, R, t_local, {"dispatch": 0.0382}, 6796.9)["dispatch"]
+    assert d["bytes"] == 2 * T * k * 4 + t_local * H * 2 + R * H * 2 + R * 4 + T * k * 4
