@@ -37,6 +37,16 @@ MUTANTS = {
                                  "if (a >= 448.0) return sign | 0x7f;"),
     "mx_round_half_away": ("double m = nearbyint(a / q);", "double m = floor(a / q + 0.5);"),
     "mx_h_not_quantised": ("mx_dequantize_row(I, hq, hs, hd);", "memcpy(hd, h, sizeof(double) * (size_t)I);"),
+    # (memory-safe mistakes only: a planted out-of-bounds index could take the test process down)
+    "up_uses_gate_weights": ("for (int h = 0; h < H; ++h) u += bf16_widen(ru[h]) * x[h];",
+                             "for (int h = 0; h < H; ++h) u += bf16_widen(rg[h]) * x[h];"),
+    "combine_first_slot_weight_for_all": ("double w = (double)topk_w[t * k + j];", "double w = (double)topk_w[t * k];"),
+    "layer_skips_first_local_expert": ("if (e < e0 || e >= e1) continue;", "if (e <= e0 || e >= e1) continue;"),
+    "grouped_row_expert_boundaries_shifted": ("if (r >= offsets[q] && r < offsets[q + 1]) { e = q; break; }",
+                                              "if (r > offsets[q] && r <= offsets[q + 1]) { e = q; break; }"),
+    "mx_amax_without_abs": ("for (int i = 0; i < len; ++i) amax = fmax(amax, fabs(v[i]));",
+                            "for (int i = 0; i < len; ++i) amax = fmax(amax, v[i]);"),
+    "e4m3_subnormal_step_halved": ("        q = ldexp(1.0, -9);", "        q = ldexp(1.0, -10);"),
 }
 
 PINS = [
@@ -53,7 +63,9 @@ PINS = [
     lambda: pf.test_combine_is_slot_ordered_weighted_gather(),
     lambda: pm.test_e4m3_table_values(),
     lambda: pm.test_nearest_code_by_exhaustive_search(),
+    lambda: pm.test_subnormal_codes_by_exhaustive_search(),
     lambda: pm.test_scale_code_closed_form(),
+    lambda: pm.test_scale_follows_largest_magnitude_of_either_sign(),
     lambda: pm.test_ties_signed_zero_and_saturation(),
     lambda: pm.test_mx_ffn_against_dequantised_float64(64, 32, 2),
     lambda: pm.test_mx_ffn_near_bf16_oracle_when_operands_are_exact(),

@@ -5,7 +5,8 @@ E4M3 elements, one UE8M0 scale per 32 elements) -- CPU only.
 - E4M3 values against the specification's table (tests/golden/e4m3_values.txt)
 - each element code is the nearest finite E4M3 value of v / X (ties to an even
   mantissa, saturating at 448), checked by exhaustive search over all codes
-- the scale code in closed form: floor(log2(amax)) - 8 + 127, 0 for a zero block
+- the scale code in closed form: floor(log2(amax)) - 8 + 127, 0 for a zero block,
+  with amax the largest magnitude of either sign (mirrored blocks share the scale)
 - the MX expert FFN against a float64 evaluation of the dequantised operands,
   and against the (separately pinned) bf16 oracle within the bound that
   quantising h implies
@@ -72,6 +73,22 @@ def test_nearest_code_by_exhaustive_search():
             assert c in cand or (best == 0 and vals[codes.index(c)] == 0), (v, t, c, cand)
 
 
+def test_subnormal_codes_by_exhaustive_search():
+    # amax 448 gives X = 2^0, so the other elements are encoded as they are: quarter steps
+    # of the subnormal quantum 2^-9 (exact codes, ties and in-between values), both signs
+    codes, vals = _all_finite_codes()
+    for sign in (1.0, -1.0):
+        elems = [sign * j * 2.0 ** -11 for j in range(1, 32)]
+        q, s = quant([448.0] + elems)
+        assert s[0, 0] == 127
+        for t, c in zip(elems, q[0, 1:]):
+            d = np.abs(vals - t)
+            cand = [codes[i] for i in np.nonzero(d == d.min())[0]]
+            if len(cand) > 1:  # a tie: the even mantissa, with the sign of t
+                cand = [cc for cc in cand if (cc & 1) == 0 and ((cc & 0x80) != 0) == (t < 0)]
+            assert c in cand or (vals[codes.index(c)] == 0 and d.min() == abs(t) and 0.0 in [vals[codes.index(cc)] for cc in cand]), (t, c, cand)
+
+
 def test_scale_code_closed_form():
     for p in range(-20, 21, 3):
         for f in (1.0, 1.25, 1.75, 1.9921875):
@@ -83,6 +100,23 @@ def test_scale_code_closed_form():
             assert oracle.mxfp8_dequantize(q, s)[0, 0] == want * 2.0 ** (p - 8)
     q, s = quant([0.0] * 32)
     assert s[0, 0] == 0 and (q == 0).all()
+
+
+def test_scale_follows_largest_magnitude_of_either_sign():
+    # OCP MX: the shared scale comes from max |v| over the block, so mirroring a block
+    # (v -> -v) keeps its scale code and flips only the sign bit of every element code
+    rng = np.random.default_rng(11)
+    for trial in range(50):
+        block = (rng.standard_normal(32) * 2.0 ** rng.uniform(-12, 12)).astype(np.float32)
+        bits = f32_to_bf16_bits(block).reshape(1, 32)
+        q, s = oracle.mxfp8_quantize(bits)
+        qn, sn = oracle.mxfp8_quantize(bits ^ np.uint16(0x8000))
+        assert np.array_equal(sn, s)
+        assert np.array_equal(qn, q ^ np.uint8(0x80))
+    # a block whose largest magnitude is negative: floor(log2 3) = 1, X = 2^-7, all exact
+    q, s = quant([-3.0, 1.0, 0.5] + [0.0] * 29)
+    assert s[0, 0] == 1 - 8 + 127
+    assert list(oracle.mxfp8_dequantize(q, s)[0, :3]) == [-3.0, 1.0, 0.5]
 
 
 def test_ties_signed_zero_and_saturation():
