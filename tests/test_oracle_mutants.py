@@ -47,6 +47,13 @@ MUTANTS = {
     "mx_amax_without_abs": ("for (int i = 0; i < len; ++i) amax = fmax(amax, fabs(v[i]));",
                             "for (int i = 0; i < len; ++i) amax = fmax(amax, v[i]);"),
     "e4m3_subnormal_step_halved": ("        q = ldexp(1.0, -9);", "        q = ldexp(1.0, -10);"),
+    "nonfinite_logits_not_detected": ("        if (!isfinite(l[e])) return ORACLE_ERR_NONFINITE;", "        (void)0;"),
+    "softmax_over_all_experts": ("for (int j = 0; j < k; ++j) s += exp((double)l[idx[j]] - m);",
+                                 "for (int j = 0; j < E; ++j) s += exp((double)l[j] - m);"),
+    "nonlocal_pair_row_zero": ("            pair_row[p] = -1;", "            pair_row[p] = 0;"),
+    "activation_without_up": ("        act[i] = silu * u;", "        act[i] = silu;"),
+    "mx_dequantise_scale_bias_126": ("out[k] = e4m3_decode(q[k]) * ldexp(1.0, (int)s[k / 32] - 127);",
+                                     "out[k] = e4m3_decode(q[k]) * ldexp(1.0, (int)s[k / 32] - 126);"),
 }
 
 PINS = [
@@ -55,6 +62,7 @@ PINS = [
     lambda: pr.test_hand_worked_example(),
     lambda: pr.test_two_expert_closed_form(),
     lambda: pr.test_weights_equal_renormalised_full_softmax(),
+    lambda: pr.test_nonfinite_logit_is_an_error(float("nan")),
     lambda: pd.test_dispatch_invariants(16, 4, 3, 11),
     lambda: pf.test_single_expert_is_textbook_mlp(),
     lambda: pf.test_identity_weights_closed_form(),
