@@ -52,6 +52,11 @@ MUTANTS = {
                                  "for (int j = 0; j < E; ++j) s += exp((double)l[j] - m);"),
     "nonlocal_pair_row_zero": ("            pair_row[p] = -1;", "            pair_row[p] = 0;"),
     "activation_without_up": ("        act[i] = silu * u;", "        act[i] = silu;"),
+    "mx_ffn_up_from_gate_weights": ("mx_dequantize_row(H, wuq + wr * H, wus + wr * (H / 32), w);",
+                                    "mx_dequantize_row(H, wgq + wr * H, wgs + wr * (H / 32), w);"),
+    "mx_ffn_silu_sign": ("h[i] = g / (1.0 + exp(-g)) * u;", "h[i] = g / (1.0 + exp(g)) * u;"),
+    "mx_ffn_gate_up_rows_of_expert_0": ("const int64_t wr = (int64_t)e * I + i;", "const int64_t wr = i;"),
+    "mx_ffn_down_rows_of_expert_0": ("const int64_t wr = (int64_t)e * H + j;", "const int64_t wr = j;"),
     "mx_dequantise_scale_bias_126": ("out[k] = e4m3_decode(q[k]) * ldexp(1.0, (int)s[k / 32] - 127);",
                                      "out[k] = e4m3_decode(q[k]) * ldexp(1.0, (int)s[k / 32] - 126);"),
 }
