@@ -52,6 +52,12 @@ MUTANTS = {
                                  "for (int j = 0; j < E; ++j) s += exp((double)l[j] - m);"),
     "nonlocal_pair_row_zero": ("            pair_row[p] = -1;", "            pair_row[p] = 0;"),
     "activation_without_up": ("        act[i] = silu * u;", "        act[i] = silu;"),
+    "layer_x_of_first_token": ("for (int h = 0; h < H; ++h) xd[h] = bf16_widen(x[t * H + h]);",
+                               "for (int h = 0; h < H; ++h) xd[h] = bf16_widen(x[h]);"),
+    "layer_first_slot_weight": ("for (int h = 0; h < H; ++h) o[h] += w[j] * y[h];",
+                                "for (int h = 0; h < H; ++h) o[h] += w[0] * y[h];"),
+    "layer_first_expert_weights": ("swiglu_ffn(H, I, xd, w_gate + (int64_t)el * I * H, w_up + (int64_t)el * I * H,",
+                                   "swiglu_ffn(H, I, xd, w_gate, w_up,"),
     "mx_ffn_up_from_gate_weights": ("mx_dequantize_row(H, wuq + wr * H, wus + wr * (H / 32), w);",
                                     "mx_dequantize_row(H, wgq + wr * H, wgs + wr * (H / 32), w);"),
     "mx_ffn_silu_sign": ("h[i] = g / (1.0 + exp(-g)) * u;", "h[i] = g / (1.0 + exp(g)) * u;"),
