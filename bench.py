@@ -8,8 +8,11 @@ workloads, its single fused launch for decode-sized ones, T*k <=
 MOE_FUSED_MAX_PAIRS).  For the split path a second loop calls the step's
 entries one by one (moe_route, moe_dispatch, moe_expert_gate_up,
 moe_expert_down, moe_combine) with CUDA events between them, for the per-kernel
-breakdown and the gate/up GEMM's roofline.  Inputs are resident in HBM; L2 is
-flushed (256 MiB write) between timed steps, outside the timed region.
+breakdown and the roofline of the two grouped GEMMs.  Inputs are resident in
+HBM; L2 is flushed (256 MiB write) between timed steps, outside the timed
+region.  After the timed region the same step runs back to back for a few
+seconds under a 100 ms nvidia-smi sampler, so that the clock record describes
+the kernels under load (the timed region itself lasts milliseconds).
 
 Prints one JSON line.  `value` is routed tokens/s (T / step time, summed over
 replicas for N > 1: every rank runs its own replica, no collective on the data
@@ -32,6 +35,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer routed tokens/s + TFLOP/s (prefill), weight GB/s (decode), 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+NOMINAL_BF16_DENSE_TFLOPS = 2250.0  # GB300 dense bf16 tensor peak, vendor figure
+LOAD_SECONDS = 3.0  # back-to-back steps under the clock sampler, outside the timed events
 L2_FLUSH_BYTES = 256 << 20
 _CS = "expert_routing_dispatch_gb300/csrc/"
 KERNEL_SOURCES = {
@@ -141,20 +146,21 @@ def recorded_traffic(kernel, config):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) during the timed region."""
+    """nvidia-smi samples (every `period_ms`) while the block runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period_ms=200):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -172,7 +178,7 @@ class ClockSampler:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
-    def summary(self):
+    def rows(self):
         rows = []
         for ln in (self.out or "").splitlines():
             f = [x.strip() for x in ln.split(",")]
@@ -183,42 +189,88 @@ class ClockSampler:
                                  pcap=f[8]))
             except ValueError:
                 continue
+        return rows
+
+    def summary(self, loaded_w=200.0):
+        """Median SM clock of the samples drawing more than `loaded_w` watts (all
+        samples if none does), the maximum clock, and every throttle reason seen."""
+        rows = self.rows()
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        loaded = [r for r in rows if r["power"] > 200] or rows
+        loaded = [r for r in rows if r["power"] > loaded_w]
         reasons = set()
         for r in rows:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
                               ("pcap", "sw_power_cap")):
                 if r[key].lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows), "power_w_max": max(r["power"] for r in rows)}
+        use = loaded or rows
+        return {"sm_mhz": statistics.median(r["sm"] for r in use), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_median_under_load": statistics.median(r["power"] for r in use),
+                "power_w_max": max(r["power"] for r in rows)}
 
 
-def cpu_baseline(cfg, inp, seconds):
-    """The oracle as it stands, on a bounded sample of the workload's tokens."""
+def clocks_record(timed, load, load_s, load_steps, kern_ms, dominant):
+    """The JSON line's clock record: the median SM clock of the samples taken while
+    the same step ran back to back for `load_s` seconds (the timed region itself is
+    too short for the 100-200 ms sampler), every throttle reason seen in either
+    window, and each dominant kernel's event time x that clock (kilocycles)."""
+    lt, tt = load.summary(loaded_w=400.0), timed.summary()
+    rec = dict(lt)
+    rec["reasons"] = sorted(set(lt.get("reasons", [])) | set(tt.get("reasons", [])) - {"no samples"})
+    rec["source"] = (f"nvidia-smi every {load.period_ms} ms while {load_steps} steps ran back to back for "
+                     f"{load_s:.1f} s after the timed region; samples above 400 W count as under load")
+    rec["timed_region"] = tt
+    if lt.get("sm_mhz"):
+        rec["kcycles_at_median_clock"] = {nm: round(kern_ms[nm] * lt["sm_mhz"], 1) for nm in dominant
+                                          if kern_ms.get(nm)}
+    return rec
+
+
+def cpu_baseline(cfg, inp, seconds, gpu_out=None):
+    """The oracle as it stands, on a bounded sample of the workload's tokens, in
+    two phases: route + dispatch over all T tokens, and the token-major layer
+    (its FFN + combine dominate) on the sample.  With `gpu_out` (the GPU's layer
+    output, host array [T, H]) the sampled tokens also give the accuracy figure
+    max |gpu - oracle| / RMS(oracle)."""
     import numpy as np
 
     import oracle
 
     T, k, e0, e1 = cfg["T"], cfg["k"], cfg["e0"], cfg["e1"]
+    t0 = time.perf_counter()
+    st, idx, _ = oracle.route(inp["logits"], k)
+    assert st == 0
+    oracle.dispatch(idx, e0, e1)
+    t_rd = time.perf_counter() - t0
 
     def run(ntok, start):
         toks = (np.arange(ntok, dtype=np.int64) + start) % T
         t0 = time.perf_counter()
-        st, _ = oracle.moe_layer_tokens(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], k, e0,
-                                        e1, tokens=toks)
+        st, ref = oracle.moe_layer_tokens(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], k, e0,
+                                          e1, tokens=toks)
         assert st == 0
-        return time.perf_counter() - t0
+        return time.perf_counter() - t0, toks, ref
 
     probe = min(T, 64)
-    dt = run(probe, 0)
+    dt, _, _ = run(probe, 0)
     n = int(min(T, max(probe, probe * seconds / max(dt, 1e-6))))
-    dt = run(n, probe)
-    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} of {T} tokens (route + SwiGLU FFN of their local slots + combine, token-major, fp64)",
-            "seconds": round(dt, 2)}
+    dt, toks, ref = run(n, probe)
+    out = {"value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "nproc": os.cpu_count(),
+           "kind": "oracle",
+           "sample": f"{n} of {T} tokens (route + SwiGLU FFN of their local slots + combine, token-major, fp64)",
+           "seconds": round(dt, 2),
+           "phases": {"route_dispatch": {"tokens": T, "seconds": round(t_rd, 4), "tokens_per_s": T / t_rd},
+                      "ffn_combine": {"tokens": n, "seconds": round(dt, 2), "tokens_per_s": n / dt,
+                                      "note": "oracle_moe_layer_tokens on the sample; its per-token routing is "
+                                              "under 0.1% of it"}}}
+    if gpu_out is not None:
+        rms = float(np.sqrt(np.mean(ref ** 2)))
+        err = float(np.abs(gpu_out[toks].astype(np.float64) - ref).max())
+        out["max_err_over_rms"] = err / rms if rms > 0 else err
+        out["accuracy_tokens"] = int(toks.size)
+    return out
 
 
 def run_reference(args):
@@ -419,6 +471,20 @@ def run_ours(args):
         for i, nm in enumerate(bnames):
             kern_ms[nm] = sum(e[i].elapsed_time(e[i + 1]) for e in b_evs) / len(b_evs)
         kern_ms["entries_total"] = sum(e[0].elapsed_time(e[-1]) for e in b_evs) / len(b_evs)
+    # clock under load: the same step back to back (no flush) with the sampler at
+    # 100 ms, outside the timed events, so the clock record describes the kernels
+    torch.cuda.synchronize()
+    load_steps = 0
+    with ClockSampler(local_rank, period_ms=100) as clk_load:
+        t_load0 = time.perf_counter()
+        while time.perf_counter() - t_load0 < LOAD_SECONDS:
+            for _ in range(20):
+                run_layer(x, lg, out, topk_idx=topk_idx, topk_w=topk_w)
+            load_steps += 20
+            torch.cuda.synchronize()
+        t_load = time.perf_counter() - t_load0
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    out_for_accuracy = None if mx else out.cpu().numpy()  # the bf16 oracle is the reference of the bf16 path
     # routed rows and active local experts, counted from this run's routing
     ti = topk_idx.flatten()
     loc = ti[(ti >= e0) & (ti < e1)]
@@ -524,12 +590,25 @@ def run_ours(args):
                     "traffic": recorded_traffic("grouped_ffn_mx", args.config),
                     "algorithmic_flop_per_launch": flop_layer}
     else:
-        achieved = flop_gate_up / (kern_ms["gate_up"] * 1e-3) / 1e12 if R else 0.0
-        roofline = {"kernel": "grouped_ffn gate/up (tcgen05, SiLU*up epilogue)", "bound": "tensor",
-                    "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
+        # both grouped GEMMs (gate/up + SiLU*up, down) against the bf16 tensor peak; the
+        # gate/up GEMM alone (the largest kernel) as a secondary figure
+        t_gemms = kern_ms["gate_up"] + kern_ms["down"]
+        achieved = flop_layer / (t_gemms * 1e-3) / 1e12 if R else 0.0
+        gu = flop_gate_up / (kern_ms["gate_up"] * 1e-3) / 1e12 if R else 0.0
+        dn = (flop_layer - flop_gate_up) / (kern_ms["down"] * 1e-3) / 1e12 if R else 0.0
+        roofline = {"kernel": "grouped_ffn gate/up (tcgen05, SiLU*up epilogue) + down, summed event times",
+                    "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
+                    "frac_of_nominal_dense": achieved / NOMINAL_BF16_DENSE_TFLOPS,
+                    "nominal_dense_peak": NOMINAL_BF16_DENSE_TFLOPS,
                     "traffic": recorded_traffic("grouped_gemm_gate_up", args.config),
-                    "algorithmic_flop_per_launch": flop_gate_up}
+                    "traffic_note": "DRAM bytes of the gate/up launch alone (ncu)",
+                    "algorithmic_flop_per_launch": flop_layer,
+                    "gate_up": {"achieved": gu, "frac": gu / peaks["bf16_tflops"],
+                                "frac_of_nominal_dense": gu / NOMINAL_BF16_DENSE_TFLOPS, "flop": flop_gate_up},
+                    "down": {"achieved": dn, "frac": dn / peaks["bf16_tflops"],
+                             "frac_of_nominal_dense": dn / NOMINAL_BF16_DENSE_TFLOPS,
+                             "flop": flop_layer - flop_gate_up}}
     gemm_ms = kern_ms["layer_fused"] if fused else kern_ms["ffn_mxfp8"] if mx else kern_ms["gate_up"] + kern_ms["down"]
     line = {
         "metric": METRIC,
@@ -556,7 +635,9 @@ def run_ours(args):
                          "expert weights resident")},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roofline,
-        "clocks": clk.summary(),
+        "clocks": clocks_record(clk, clk_load, t_load, load_steps, kern_ms,
+                                [nm for nm in ("gate_up", "down", "layer", "layer_fused", "layer_mxfp8",
+                                               "ffn_mxfp8") if nm in kern_ms]),
         "detail": {
             "kernel_ms": {nm: round(v, 4) for nm, v in kern_ms.items()},
             "layer_tflops": flop_layer / (t_step * 1e-3) / 1e12,
@@ -572,7 +653,9 @@ def run_ours(args):
         },
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_seconds, gpu_out=out_for_accuracy)
+        if "max_err_over_rms" in line["cpu_baseline"]:
+            line["max_err_over_rms"] = line["cpu_baseline"]["max_err_over_rms"]
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -15,7 +15,7 @@ __all__ = [
     "moe_layer", "moe_combine_accumulate", "moe_expert_gate_up", "moe_expert_down", "moe_workspace_size", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
     "moe_status_string", "alloc_workspace", "EXPORTED", "moe_testing_layer_stalled_barrier", "FUSED_MAX_PAIRS",
     "moe_quantize_mxfp8", "moe_expert_ffn_mxfp8_workspace_size", "moe_expert_ffn_mxfp8", "moe_layer_mxfp8_workspace_size",
-    "moe_layer_mxfp8",
+    "moe_layer_mxfp8", "moe_testing_expert_gate_up_stalled", "moe_testing_expert_ffn_mxfp8_stalled",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +26,8 @@ EXPORTED = ("moe_status_string", "moe_dispatch_workspace_size", "moe_expert_ffn_
             "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_expert_gate_up",
             "moe_expert_down", "moe_combine", "moe_combine_accumulate", "moe_layer",
             "moe_testing_layer_stalled_barrier", "moe_quantize_mxfp8", "moe_expert_ffn_mxfp8_workspace_size",
-            "moe_expert_ffn_mxfp8", "moe_layer_mxfp8_workspace_size", "moe_layer_mxfp8")
+            "moe_expert_ffn_mxfp8", "moe_layer_mxfp8_workspace_size", "moe_layer_mxfp8",
+            "moe_testing_expert_gate_up_stalled", "moe_testing_expert_ffn_mxfp8_stalled")
 
 FUSED_MAX_PAIRS = 8192  # MOE_FUSED_MAX_PAIRS in include/moe.h
 
@@ -83,6 +84,7 @@ def lib():
         L.moe_dispatch_noalloc.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_ffn.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         L.moe_expert_gate_up.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_testing_expert_gate_up_stalled.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_down.argtypes = [pd, vp, vp, vp, vp, vp, vp]
         L.moe_combine.argtypes = [pd, vp, vp, vp, vp, vp]
         L.moe_combine_accumulate.argtypes = [pd, vp, vp, vp, vp, vp]
@@ -90,10 +92,12 @@ def lib():
         L.moe_testing_layer_stalled_barrier.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         L.moe_quantize_mxfp8.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, vp, vp, vp]
         L.moe_expert_ffn_mxfp8.argtypes = [pd] + [vp] * 11 + [sz, vp, vp]
+        L.moe_testing_expert_ffn_mxfp8_stalled.argtypes = [pd] + [vp] * 11 + [sz, vp, vp]
         L.moe_layer_mxfp8.argtypes = [pd] + [vp] * 12 + [sz, vp, vp]
         for f in (L.moe_route, L.moe_dispatch, L.moe_dispatch_noalloc, L.moe_expert_ffn, L.moe_expert_gate_up, L.moe_expert_down,
                   L.moe_combine, L.moe_combine_accumulate, L.moe_layer, L.moe_testing_layer_stalled_barrier,
-                  L.moe_quantize_mxfp8, L.moe_expert_ffn_mxfp8, L.moe_layer_mxfp8):
+                  L.moe_quantize_mxfp8, L.moe_expert_ffn_mxfp8, L.moe_layer_mxfp8,
+                  L.moe_testing_expert_gate_up_stalled, L.moe_testing_expert_ffn_mxfp8_stalled):
             f.restype = i32
         _lib = L
     return _lib
@@ -189,6 +193,15 @@ def moe_expert_gate_up(dims, x_perm, offsets, w_gate, w_up, h, status=None, stre
                                     _ptr(status), _stream(stream)), "moe_expert_gate_up")
 
 
+def moe_testing_expert_gate_up_stalled(dims, x_perm, offsets, w_gate, w_up, h, status=None, stream=None):
+    """Fault-injection hook: moe_expert_gate_up whose first ring stage never fills;
+    the kernel must report MOE_ERR_TIMEOUT in `status` and return."""
+    d = Dims.of(dims)
+    _check(lib().moe_testing_expert_gate_up_stalled(ctypes.byref(d), _ptr(x_perm), _ptr(offsets), _ptr(w_gate),
+                                                    _ptr(w_up), _ptr(h), _ptr(status), _stream(stream)),
+           "moe_testing_expert_gate_up_stalled")
+
+
 def moe_expert_down(dims, h, offsets, w_down, y_perm, status=None, stream=None):
     d = Dims.of(dims)
     _check(lib().moe_expert_down(ctypes.byref(d), _ptr(h), _ptr(offsets), _ptr(w_down), _ptr(y_perm), _ptr(status),
@@ -250,6 +263,19 @@ def moe_expert_ffn_mxfp8(dims, x_perm_q, x_perm_s, offsets, w_gate, w_up, w_down
                                       _ptr(w_gate[0]), _ptr(w_gate[1]), _ptr(w_up[0]), _ptr(w_up[1]),
                                       _ptr(w_down[0]), _ptr(w_down[1]), _ptr(y_perm), _ptr(ws), nb, _ptr(status),
                                       _stream(stream)), "moe_expert_ffn_mxfp8")
+
+
+def moe_testing_expert_ffn_mxfp8_stalled(dims, x_perm_q, x_perm_s, offsets, w_gate, w_up, w_down, y_perm, ws,
+                                         ws_bytes=None, status=None, stream=None):
+    """Fault-injection hook: moe_expert_ffn_mxfp8 whose gate/up ring never fills its
+    first stage; the kernel must report MOE_ERR_TIMEOUT in `status` and return."""
+    d = Dims.of(dims)
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check(lib().moe_testing_expert_ffn_mxfp8_stalled(ctypes.byref(d), _ptr(x_perm_q), _ptr(x_perm_s),
+                                                      _ptr(offsets), _ptr(w_gate[0]), _ptr(w_gate[1]),
+                                                      _ptr(w_up[0]), _ptr(w_up[1]), _ptr(w_down[0]),
+                                                      _ptr(w_down[1]), _ptr(y_perm), _ptr(ws), nb, _ptr(status),
+                                                      _stream(stream)), "moe_testing_expert_ffn_mxfp8_stalled")
 
 
 def moe_layer_mxfp8(dims, x, logits, w_gate, w_up, w_down, out, ws, ws_bytes=None, topk_idx=None, topk_w=None,

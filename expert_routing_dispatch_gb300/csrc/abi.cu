@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/moe.h"
 #include "kernels.h"
 
@@ -14,6 +16,27 @@ int sm_count() {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     return n > 0 ? n : 1;
+}
+
+cudaError_t ensure_dynamic_smem(const void* func, int bytes) {
+    constexpr int kSlots = 256;
+    static std::mutex mu;
+    static const void* seen_func[kSlots];
+    static int seen_dev[kSlots];
+    static int nseen = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < nseen; ++i)
+        if (seen_func[i] == func && seen_dev[i] == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && nseen < kSlots) {  // a full table only means the call repeats
+        seen_func[nseen] = func;
+        seen_dev[nseen] = dev;
+        ++nseen;
+    }
+    return e;
 }
 
 namespace {
@@ -230,15 +253,26 @@ int moe_expert_ffn(const moe_dims* d, const uint16_t* x_perm, const int32_t* off
                                       d->I, d->e1 - d->e0, ws, status_dev, (cudaStream_t)stream));
 }
 
-int moe_expert_gate_up(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
-                       const uint16_t* w_up, uint16_t* h, int32_t* status_dev, void* stream) {
+static int gate_up_impl(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
+                        const uint16_t* w_up, uint16_t* h, int32_t* status_dev, void* stream, int stall) {
     int st = check_dims(d);
     if (st) return st;
     if (!aligned16(x_perm) || !aligned16(offsets) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(h))
         return MOE_ERR_INVALID_ARG;
     if ((st = check_device())) return st;
     return launched(launch_gate_up(x_perm, offsets, w_gate, w_up, h, (long long)pairs_of(d), d->H, d->I,
-                                   d->e1 - d->e0, status_dev, (cudaStream_t)stream));
+                                   d->e1 - d->e0, status_dev, (cudaStream_t)stream, stall));
+}
+
+int moe_expert_gate_up(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
+                       const uint16_t* w_up, uint16_t* h, int32_t* status_dev, void* stream) {
+    return gate_up_impl(d, x_perm, offsets, w_gate, w_up, h, status_dev, stream, 0);
+}
+
+int moe_testing_expert_gate_up_stalled(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets,
+                                       const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,
+                                       int32_t* status_dev, void* stream) {
+    return gate_up_impl(d, x_perm, offsets, w_gate, w_up, h, status_dev, stream, 1);
 }
 
 int moe_expert_down(const moe_dims* d, const uint16_t* h, const int32_t* offsets, const uint16_t* w_down,
@@ -338,10 +372,11 @@ size_t moe_expert_ffn_mxfp8_workspace_size(const moe_dims* d) {
     return align_up(mx_ffn_scratch_bytes((long long)pairs_of(d), d->I));
 }
 
-int moe_expert_ffn_mxfp8(const moe_dims* d, const uint8_t* x_perm_q, const uint8_t* x_perm_s, const int32_t* offsets,
-                         const uint8_t* w_gate_q, const uint8_t* w_gate_s, const uint8_t* w_up_q,
-                         const uint8_t* w_up_s, const uint8_t* w_down_q, const uint8_t* w_down_s, float* y_perm,
-                         void* ws, size_t ws_bytes, int32_t* status_dev, void* stream) {
+static int ffn_mxfp8_impl(const moe_dims* d, const uint8_t* x_perm_q, const uint8_t* x_perm_s,
+                          const int32_t* offsets, const uint8_t* w_gate_q, const uint8_t* w_gate_s,
+                          const uint8_t* w_up_q, const uint8_t* w_up_s, const uint8_t* w_down_q,
+                          const uint8_t* w_down_s, float* y_perm, void* ws, size_t ws_bytes, int32_t* status_dev,
+                          void* stream, int stall) {
     int st = check_mx_dims(d);
     if (st) return st;
     const void* ptrs[] = {x_perm_q, x_perm_s, offsets, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q, w_down_s, y_perm};
@@ -351,7 +386,24 @@ int moe_expert_ffn_mxfp8(const moe_dims* d, const uint8_t* x_perm_q, const uint8
     if ((st = check_device())) return st;
     return launched(launch_mx_expert_ffn(x_perm_q, x_perm_s, offsets, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q,
                                          w_down_s, y_perm, (long long)pairs_of(d), d->H, d->I, d->e1 - d->e0, ws,
-                                         status_dev, (cudaStream_t)stream));
+                                         status_dev, (cudaStream_t)stream, stall));
+}
+
+int moe_expert_ffn_mxfp8(const moe_dims* d, const uint8_t* x_perm_q, const uint8_t* x_perm_s, const int32_t* offsets,
+                         const uint8_t* w_gate_q, const uint8_t* w_gate_s, const uint8_t* w_up_q,
+                         const uint8_t* w_up_s, const uint8_t* w_down_q, const uint8_t* w_down_s, float* y_perm,
+                         void* ws, size_t ws_bytes, int32_t* status_dev, void* stream) {
+    return ffn_mxfp8_impl(d, x_perm_q, x_perm_s, offsets, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q, w_down_s,
+                          y_perm, ws, ws_bytes, status_dev, stream, 0);
+}
+
+int moe_testing_expert_ffn_mxfp8_stalled(const moe_dims* d, const uint8_t* x_perm_q, const uint8_t* x_perm_s,
+                                         const int32_t* offsets, const uint8_t* w_gate_q, const uint8_t* w_gate_s,
+                                         const uint8_t* w_up_q, const uint8_t* w_up_s, const uint8_t* w_down_q,
+                                         const uint8_t* w_down_s, float* y_perm, void* ws, size_t ws_bytes,
+                                         int32_t* status_dev, void* stream) {
+    return ffn_mxfp8_impl(d, x_perm_q, x_perm_s, offsets, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q, w_down_s,
+                          y_perm, ws, ws_bytes, status_dev, stream, 1);
 }
 
 size_t moe_layer_mxfp8_workspace_size(const moe_dims* d) {

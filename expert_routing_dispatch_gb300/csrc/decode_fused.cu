@@ -276,8 +276,8 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
                                uint16_t* x_perm, uint16_t* h, float* y_perm, unsigned* sync, int T, int H, int I,
                                int E, int k, int e0, int e1, int32_t* status, int stall_first_barrier,
                                cudaStream_t s) {
-    static cudaError_t attr = cudaFuncSetAttribute(moe_layer_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)FUSED_SMEM_BYTES);
+    const cudaError_t attr =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(&moe_layer_fused_kernel), (int)FUSED_SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
     const int n = e1 - e0;
     const long long rows = (long long)T * k;

@@ -51,21 +51,37 @@ __global__ void __launch_bounds__(256) dispatch_count_kernel(const int32_t* __re
     for (int e = threadIdx.x; e < n; e += blockDim.x) chunk_hist[(size_t)blockIdx.x * n + e] = hist[e];
 }
 
-// one CTA: thread e owns local expert e
+// one CTA of 1024 threads.  Pass 1: warp w scans the chunk column of experts w,
+// w + 32, ... (exclusive within the expert, in place, 32 chunks per step) and
+// records the expert's total; then a block scan of the totals gives the offsets;
+// pass 2 adds each expert's offset to its column.  Work per thread is at most
+// n * nchunks / 1024 entries.
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int n,
                                                              int32_t* __restrict__ counts,
                                                              int32_t* __restrict__ offsets) {
+    __shared__ int tot[kMaxLocal];
     __shared__ int warp_tot[32];
-    const int e = threadIdx.x;
-    int total = 0;
-    if (e < n)
-        for (int c = 0; c < nchunks; ++c) {
-            int v = chunk_hist[(size_t)c * n + e];
-            chunk_hist[(size_t)c * n + e] = total;  // exclusive within the expert
-            total += v;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = warp; e < n; e += 32) {
+        int carry = 0;
+        for (int c0 = 0; c0 < nchunks; c0 += 32) {
+            const int c = c0 + lane;
+            const int v = c < nchunks ? chunk_hist[(size_t)c * n + e] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (c < nchunks) chunk_hist[(size_t)c * n + e] = carry + incl - v;  // exclusive within the expert
+            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-    // block exclusive scan of totals over e
-    const int lane = e & 31, warp = e >> 5;
+        if (lane == 0) tot[e] = carry;
+    }
+    __syncthreads();
+    // block exclusive scan of the totals over e (thread e)
+    const int e = threadIdx.x;
+    const int total = e < n ? tot[e] : 0;
     int incl = total;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -84,12 +100,17 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict
         warp_tot[lane] = v;  // inclusive over warps
     }
     __syncthreads();
-    int excl = incl - total + (warp > 0 ? warp_tot[warp - 1] : 0);
+    const int excl = incl - total + (warp > 0 ? warp_tot[warp - 1] : 0);
     if (e < n) {
         counts[e] = total;
         offsets[e] = excl;
         if (e == n - 1) offsets[n] = excl + total;
-        for (int c = 0; c < nchunks; ++c) chunk_hist[(size_t)c * n + e] += excl;
+        tot[e] = excl;
+    }
+    __syncthreads();
+    for (int e2 = warp; e2 < n; e2 += 32) {
+        const int base = tot[e2];
+        for (int c = lane; c < nchunks; c += 32) chunk_hist[(size_t)c * n + e2] += base;
     }
 }
 
@@ -367,21 +388,57 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_noalloc_chunk_hist on the current device, looked up once
-// per device (host code cannot use the symbol's host-side shadow as a pointer).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if there is none or the
+// driver cannot tell).  Ids are never reused within a process, so a context
+// rebuilt after cudaDeviceReset gets a new one.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    static CtxGetIdFn get_id = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<CtxGetIdFn>(p);
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_noalloc_chunk_hist on the current device.  Host code
+// cannot use the symbol's host-side shadow as a pointer, so the address is looked
+// up with cudaGetSymbolAddress once per device and context: a context rebuilt
+// after cudaDeviceReset (a new context id) gets a fresh lookup instead of a stale
+// address.
 cudaError_t noalloc_scratch(int32_t** out) {
     static std::mutex mu;
     static int32_t* addr[kMaxDevices] = {};
+    static unsigned long long ctx_of_addr[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!addr[dev] || ctx == 0 || ctx != ctx_of_addr[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_chunk_hist);
         if (e != cudaSuccess) return e;
         addr[dev] = static_cast<int32_t*>(p);
+        ctx_of_addr[dev] = current_context_id();  // the lookup made the device's context current
     }
     *out = addr[dev];
     return cudaSuccess;

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     Ctl& c = ctl_of(smem_raw);
     const int n = args.g.n;
 
-    init(c);
+    init(c, args.g.stall);
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
         for (int i = 0; i < 3; ++i) {
@@ -109,9 +109,7 @@ namespace {
 
 template <int MODE>
 cudaError_t set_smem_attr() {
-    static cudaError_t err = cudaFuncSetAttribute(grouped_ffn_kernel<MODE>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    return err;
+    return ensure_dynamic_smem(reinterpret_cast<const void*>(&grouped_ffn_kernel<MODE>), (int)SMEM_BYTES);
 }
 
 }  // namespace
@@ -120,14 +118,15 @@ size_t ffn_scratch_bytes(long long rows, int I) { return (size_t)rows * (size_t)
 
 cudaError_t launch_gate_up(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
                            const uint16_t* w_up, uint16_t* h, long long rows, int H, int I, int n, int32_t* status,
-                           cudaStream_t s) {
+                           cudaStream_t s, int stall) {
     cudaError_t e;
     if ((e = set_smem_attr<MODE_GATEUP>()) != cudaSuccess) return e;
     CUtensorMap mA;
     WMaps wm;
     if (!make_tmap_bf16(&mA, x_perm, rows, H, BM) || !make_wmaps(&wm, w_gate, w_up, (long long)n * I, H, BN / 2))
         return cudaErrorInvalidValue;
-    FfnArgs a{offsets, {h, status, n, H / BK, (I + BN / 2 - 1) / (BN / 2), I, I, BN / 2, kPrefetchGateUp, BN, 0}};
+    FfnArgs a{offsets,
+              {h, status, n, H / BK, (I + BN / 2 - 1) / (BN / 2), I, I, BN / 2, kPrefetchGateUp, BN, 0, stall}};
     grouped_ffn_kernel<MODE_GATEUP><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mA, wm, a);
     return cudaGetLastError();
 }

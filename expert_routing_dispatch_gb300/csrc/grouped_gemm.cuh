@@ -107,6 +107,7 @@ struct Args {
     int prefetch;     // L2 prefetch distance of the weight boxes in k-blocks (0 = off)
     int bn;           // MMA N = weight rows per tile (256; 128 also supported)
     int a_small;      // box rows of the optional small token map (0 = none)
+    int stall;        // testing hook: extra arrivals ring stage 0 waits for (0 in normal use)
 };
 
 // Per-thread pipeline counters; they carry over from one GEMM phase to the next
@@ -136,12 +137,14 @@ __device__ __forceinline__ Ctl& ctl_of(uint8_t* raw) {
     return *reinterpret_cast<Ctl*>(raw + (b - smem_u32(raw)) + (size_t)STAGES * STAGE_BYTES);
 }
 
-// thread 0: barriers; warp 1: TMEM.  Caller syncs afterwards.
-__device__ __forceinline__ void init(Ctl& c) {
+// thread 0: barriers; warp 1: TMEM.  Caller syncs afterwards.  `stall` > 0 (a
+// testing hook) makes stage 0's `full` barrier wait for arrivals that never come,
+// so the MMA warp's bounded wait runs out and the timeout path is exercised.
+__device__ __forceinline__ void init(Ctl& c, int stall = 0) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&c.full[s]), 1);
+            mbar_init(smem_u32(&c.full[s]), 1 + (s == 0 ? stall : 0));
             mbar_init(smem_u32(&c.empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {

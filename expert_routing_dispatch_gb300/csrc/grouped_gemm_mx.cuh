@@ -101,6 +101,7 @@ struct Args {
     int out_cols;            // I (gate/up) or H (down)
     int w_rows;              // weight rows per expert (I or H)
     int n_step;              // output columns per n-tile: 96 (gate/up) or 192 (down)
+    int stall;               // testing hook: extra arrivals ring stage 0 waits for (0 in normal use)
 };
 
 struct TileCoord {
@@ -168,11 +169,13 @@ __device__ __forceinline__ uint32_t mx_quantize32(const float (&v)[32], uint32_t
     return code;
 }
 
-__device__ __forceinline__ void init(Ctl& c) {
+// `stall` > 0 (a testing hook) makes stage 0's `full` barrier wait for arrivals
+// that never come, so the MMA warp's bounded wait runs out.
+__device__ __forceinline__ void init(Ctl& c, int stall = 0) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&c.full[s]), 2);
+            mbar_init(smem_u32(&c.full[s]), 2 + (s == 0 ? stall : 0));
             mbar_init(smem_u32(&c.empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {

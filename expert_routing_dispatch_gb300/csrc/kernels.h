@@ -43,9 +43,11 @@ cudaError_t launch_expert_ffn(const uint16_t* x_perm, const int32_t* offsets, co
                               const uint16_t* w_up, const uint16_t* w_down, float* y_perm, long long rows, int H,
                               int I, int n, void* scratch, int32_t* status, cudaStream_t s);
 
+// stall > 0: testing hook, the GEMM's first ring stage never completes (bounded
+// waits run out, the status word gets MOE_ERR_TIMEOUT)
 cudaError_t launch_gate_up(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
                            const uint16_t* w_up, uint16_t* h, long long rows, int H, int I, int n, int32_t* status,
-                           cudaStream_t s);
+                           cudaStream_t s, int stall = 0);
 cudaError_t launch_down(const uint16_t* h, const int32_t* offsets, const uint16_t* w_down, float* y_perm,
                         long long rows, int H, int I, int n, int32_t* status, cudaStream_t s);
 
@@ -76,9 +78,14 @@ size_t mx_ffn_scratch_bytes(long long rows, int I);  // h codes + h scales
 cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets, const uint8_t* wgq,
                                  const uint8_t* wgs, const uint8_t* wuq, const uint8_t* wus, const uint8_t* wdq,
                                  const uint8_t* wds, float* y_perm, long long rows, int H, int I, int n,
-                                 void* scratch, int32_t* status, cudaStream_t s);
+                                 void* scratch, int32_t* status, cudaStream_t s, int stall_gate_up = 0);
 
 // device query shared by the launchers
 int sm_count();
+
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) on the current
+// device, once per (kernel, device): the attribute belongs to the device's copy
+// of the kernel, so a process that drives several GPUs sets it on each of them.
+cudaError_t ensure_dynamic_smem(const void* func, int bytes);
 
 }  // namespace moe

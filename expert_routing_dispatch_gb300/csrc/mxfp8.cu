@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
     const uint32_t ring = mx::ring_base(smem_raw);
     mx::Ctl& c = mx::ctl_of(smem_raw);
     const int n = args.n;
-    mx::init(c);
+    mx::init(c, args.stall);
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB0);
@@ -125,8 +125,8 @@ bool make_tmap_u8(CUtensorMap* m, const void* ptr, long long rows, int cols, int
 template <int MODE>
 cudaError_t launch_mx_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                            const int32_t* offsets, const mx::Args& args, cudaStream_t s) {
-    static cudaError_t attr = cudaFuncSetAttribute(grouped_ffn_mx_kernel<MODE>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx::SMEM_BYTES);
+    const cudaError_t attr =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(&grouped_ffn_mx_kernel<MODE>), (int)mx::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
     grouped_ffn_mx_kernel<MODE><<<sm_count(), mx::NUM_THREADS, mx::SMEM_BYTES, s>>>(a, b0, b1, offsets, args);
     return cudaGetLastError();
@@ -159,7 +159,7 @@ size_t mx_ffn_scratch_bytes(long long rows, int I) {
 cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets, const uint8_t* wgq,
                                  const uint8_t* wgs, const uint8_t* wuq, const uint8_t* wus, const uint8_t* wdq,
                                  const uint8_t* wds, float* y_perm, long long rows, int H, int I, int n,
-                                 void* scratch, int32_t* status, cudaStream_t s) {
+                                 void* scratch, int32_t* status, cudaStream_t s, int stall_gate_up) {
     uint8_t* hq = static_cast<uint8_t*>(scratch);
     uint8_t* hs = hq + align256((size_t)rows * (size_t)I);
     const int nt_gu = (I + mx::BN / 2 - 1) / (mx::BN / 2), nt_dn = (H + mx::BN - 1) / mx::BN;
@@ -180,7 +180,8 @@ cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int
                       nt_gu,
                       I,
                       I,
-                      mx::BN / 2};
+                      mx::BN / 2,
+                      stall_gate_up};
     cudaError_t e = launch_mx_gemm<mx::MODE_GATEUP>(mX, mG, mU, offsets, ga, s);
     if (e != cudaSuccess) return e;
     const mx::Args da{y_perm,
@@ -195,7 +196,8 @@ cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int
                       nt_dn,
                       H,
                       H,
-                      mx::BN};
+                      mx::BN,
+                      0};
     return launch_mx_gemm<mx::MODE_DOWN>(mH, mD, mD, offsets, da, s);
 }
 

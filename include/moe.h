@@ -119,10 +119,15 @@ int moe_dispatch(const moe_dims* d, const uint16_t* x, const int32_t* topk_idx,
  * process exits.  Limit: ceil(T*k / 2048) * (e1 - e0) <= 262144, e.g. T*k up to
  * 4,194,304 pairs with 128 local experts; larger problems return
  * MOE_ERR_UNSUPPORTED without launching.  It never calls cudaMalloc or cudaFree.
- * The first call on each device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  All calls
- * share the one array: calls whose work overlaps on the GPU (for instance on two
- * streams) race and give undefined results; calls ordered on one stream are fine.
+ * The first call on each device (with that device current) looks up the array's
+ * device address with cudaGetSymbolAddress, which allocates nothing, and keeps it
+ * for that device's context; the first call after a cudaDeviceReset looks it up
+ * again.  That lookup may load the library's device code, so make the first call
+ * on each device (and after a reset) before any stream capture.
+ * All calls share the one array: calls whose work overlaps on the GPU (for
+ * instance on two streams) race and give undefined results; calls ordered on one
+ * stream are fine.  Its scan step reads n * ceil(T*k / 2048) histogram entries,
+ * one warp per local expert; at the size limit that is 262144 entries.
  */
 int moe_dispatch_noalloc(const moe_dims* d, const uint16_t* x, const int32_t* topk_idx,
                          int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
@@ -157,6 +162,19 @@ int moe_expert_gate_up(const moe_dims* d, const uint16_t* x_perm, const int32_t*
                        int32_t* status_dev, void* stream);
 int moe_expert_down(const moe_dims* d, const uint16_t* h, const int32_t* offsets,
                     const uint16_t* w_down, float* y_perm, int32_t* status_dev, void* stream);
+
+/*
+ * Testing hook for failure detection without a GPU fault: moe_expert_gate_up
+ * with the first stage of every CTA's shared-memory ring told to wait for one
+ * arrival more than is ever made.  The MMA warp's bounded wait on that stage runs
+ * out (~1 s of GPU clock cycles); the kernel writes MOE_ERR_TIMEOUT to
+ * *status_dev, stops every role, waits (bounded) for its own copies in flight,
+ * frees its tensor memory and returns, and the CUDA context stays usable.  h is
+ * undefined afterwards.  Arguments as for moe_expert_gate_up.
+ */
+int moe_testing_expert_gate_up_stalled(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets,
+                                       const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,
+                                       int32_t* status_dev, void* stream);
 
 /*
  * Combine ("Expert Parallel" and "MoE Dispatch - Combine" sections: weighted
@@ -249,6 +267,18 @@ int moe_expert_ffn_mxfp8(const moe_dims* d, const uint8_t* x_perm_q, const uint8
                          const uint8_t* w_gate_q, const uint8_t* w_gate_s, const uint8_t* w_up_q,
                          const uint8_t* w_up_s, const uint8_t* w_down_q, const uint8_t* w_down_s, float* y_perm,
                          void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
+ * Testing hook, as moe_testing_expert_gate_up_stalled for the MXFP8 FFN: its
+ * gate/up GEMM's first ring stage waits for an arrival that never comes, so the
+ * MMA warp's bounded wait runs out and *status_dev gets MOE_ERR_TIMEOUT; the down
+ * GEMM then runs on an undefined h.  Arguments as for moe_expert_ffn_mxfp8.
+ */
+int moe_testing_expert_ffn_mxfp8_stalled(const moe_dims* d, const uint8_t* x_perm_q, const uint8_t* x_perm_s,
+                                         const int32_t* offsets, const uint8_t* w_gate_q, const uint8_t* w_gate_s,
+                                         const uint8_t* w_up_q, const uint8_t* w_up_s, const uint8_t* w_down_q,
+                                         const uint8_t* w_down_s, float* y_perm, void* ws, size_t ws_bytes,
+                                         int32_t* status_dev, void* stream);
 
 /*
  * The whole local layer with MXFP8 expert weights: route, dispatch (x quantised to

@@ -66,6 +66,38 @@ def sample_rows(offsets, n_per_expert=3, extra=64, seed=0):
     return np.unique(np.asarray(rows, dtype=np.int64))
 
 
+def parity_rows(offsets, at_least=2048, seed=0):
+    """Grouped rows for a parity check: every row when R <= at_least; else the
+    first, middle and last row of every non-empty expert plus seeded rows, at
+    least `at_least` distinct rows in all."""
+    off = np.asarray(offsets, np.int64)
+    R = int(off[-1])
+    if R <= at_least:
+        return np.arange(R, dtype=np.int64)
+    rows = set()
+    for e in range(off.size - 1):
+        if off[e + 1] > off[e]:
+            rows.update((int(off[e]), int((off[e] + off[e + 1]) // 2), int(off[e + 1] - 1)))
+    draw = 0
+    while len(rows) < at_least:
+        rows.update(int(r) for r in synth.uniform_int(seed + draw, synth.TID_AUX + 8, at_least, R))
+        draw += 1
+    return np.asarray(sorted(rows), dtype=np.int64)
+
+
+def parity_tokens(T, at_least=2048, seed=0):
+    """Every token when T <= at_least, else the first, the last and seeded others,
+    at least `at_least` distinct tokens in all."""
+    if T <= at_least:
+        return np.arange(T, dtype=np.int64)
+    toks = {0, T - 1}
+    draw = 0
+    while len(toks) < at_least:
+        toks.update(int(t) for t in synth.uniform_int(seed + draw, synth.TID_AUX + 7, at_least, T))
+        draw += 1
+    return np.asarray(sorted(toks), dtype=np.int64)
+
+
 def bf16_h_bound(inp, k, e0, e1, tokens, idx, w):
     """Elementwise bound of |gpu - oracle| implied by the GPU's arithmetic: h is
     rounded to bf16 (unit roundoff u = 2^-8) before the down GEMM, everything

@@ -80,3 +80,26 @@ def test_memory_bound_rates_prefill_ep_rank_numbers():
     assert abs(r["combine"]["frac_of_hbm"] - r["combine"]["gbs"] / 6796.9) < 1e-4
     d = bench.memory_bound_rates(T, E, k, H, R, t_local, {"dispatch": 0.0382}, 6796.9)["dispatch"]
     assert d["bytes"] == 2 * T * k * 4 + t_local * H * 2 + R * H * 2 + R * 4 + T * k * 4
+
+
+def test_clock_record_uses_the_load_window():
+    # fake nvidia-smi output: the timed region saw two idle samples, the load loop
+    # six samples at dense-GEMM power and one idle; reasons from both windows count
+    sys.path.insert(0, ROOT)
+    import bench
+
+    def sampler(lines, period):
+        c = bench.ClockSampler(0, period_ms=period)
+        c.out = "\n".join(lines)
+        return c
+
+    idle = "0, 2070, 2070, 180.5, 0x0, Not Active, Not Active, Not Active, Not Active"
+    timed = sampler([idle, idle], 200)
+    load = sampler([idle] + [f"0, {m}, 2070, {p}, 0x4, Not Active, Not Active, Not Active, Active"
+                             for m, p in ((1650, 1390), (1700, 1380), (1680, 1395), (1720, 1370), (1690, 1385),
+                                          (1710, 1388))], 100)
+    rec = bench.clocks_record(timed, load, 3.0, 120, {"gate_up": 0.25, "down": 0.14}, ["gate_up", "down"])
+    assert rec["samples_under_load"] == 6 and rec["sm_mhz"] == 1695.0
+    assert rec["reasons"] == ["sw_power_cap"]
+    assert rec["timed_region"]["samples"] == 2
+    assert rec["kcycles_at_median_clock"] == {"gate_up": round(0.25 * 1695.0, 1), "down": round(0.14 * 1695.0, 1)}

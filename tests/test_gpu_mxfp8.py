@@ -12,13 +12,16 @@ Bars:
   RMS, i.e. fp32 accumulation (a wrong scale anywhere would be a factor of 2);
 - the expert FFN and the layer against the oracle's own MXFP8 pipeline: within
   2e-2 * RMS; routing bit-exact.
+The FFN is checked on at least 2048 grouped rows per workload (all rows when there
+are fewer, always the first, middle and last row of every expert), the layer on at
+least 2048 tokens (all of them when there are fewer).
 """
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_helpers import dev, host, inputs, oracle_routing, rel_err, sample_rows, sample_tokens
+from gpu_helpers import dev, host, inputs, oracle_routing, parity_rows, parity_tokens, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -124,7 +127,7 @@ def run_ffn(moe, name):
 def test_mx_expert_ffn(moe, name):
     cfg, d, xq, xs, w, y, hq, hs = run_ffn(moe, name)
     R = d["R"]
-    rows = sample_rows(d["offsets"], extra=48 if R > 4096 else R)
+    rows = parity_rows(d["offsets"], at_least=2048)
     if rows.size == 0:
         return
     args = (xq, xs, d["offsets"], w["w_gate"], w["w_up"], w["w_down"], rows)
@@ -141,7 +144,7 @@ def test_mx_expert_ffn(moe, name):
     # the down GEMM alone, and the whole FFN against the oracle's own MXFP8 pipeline
     e_down, rms_down = rel_err(y[rows], y_gpu_h)
     e_all, rms_all = rel_err(y[rows], y_own)
-    print(f"PARITY mxfp8 ffn {cfg['name']} h code flips {flips:.4%}, down-only max/RMS {e_down / rms_down:.2e}, "
+    print(f"PARITY mxfp8 ffn {cfg['name']} rows {rows.size} of {R}: h code flips {flips:.4%}, down-only max/RMS {e_down / rms_down:.2e}, "
           f"ffn max/RMS {e_all / rms_all:.2e}")
     assert flips < 0.02
     assert e_down <= 1e-3 * rms_down
@@ -167,7 +170,7 @@ def test_mx_layer(moe, name):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert np.array_equal(host(idx), idx_o)
-    toks = sample_tokens(T, 48)
+    toks = parity_tokens(T, 2048)
     # oracle: MXFP8 FFN of every local slot of the sampled tokens, combined in slot order
     xq_t, xs_t = oracle.mxfp8_quantize(inp["x"])
     P = T * k
@@ -190,7 +193,7 @@ def test_mx_layer(moe, name):
     st, ref16 = oracle.moe_layer_tokens(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], k, e0, e1,
                                         tokens=toks)
     e16, rms16 = rel_err(got, ref16)
-    print(f"PARITY mxfp8 layer {name} max|gpu-oracle_mx|/RMS = {err / rms:.3e} (vs the bf16 oracle: "
+    print(f"PARITY mxfp8 layer {name} tokens {toks.size} of {T}: max|gpu-oracle_mx|/RMS = {err / rms:.3e} (vs the bf16 oracle: "
           f"{e16 / rms16:.3e})")
     assert err <= 2e-2 * rms
 

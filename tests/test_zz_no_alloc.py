@@ -64,11 +64,22 @@ def _dispatch_both(moe, cfg):
 
 
 def test_noalloc_dispatch_matches_dispatch_on_two_calls_in_a_row(moe):
-    # first a large problem that fills much of the array, then a smaller one with
-    # a different local range: leftovers from the first call must not leak
+    # first the 16384-token workload (64 chunks x 128 experts = 8192 of the array's
+    # 262144 entries), then a smaller one with a different local range: leftovers
+    # from the first call must not leak
     r1 = _dispatch_both(moe, synth.config("prefill_full"))
     r2 = _dispatch_both(moe, synth.config("skewed_rank0"))
     assert r1 == 16384 * 8 and r2 > 0
+
+
+def test_noalloc_dispatch_at_the_size_limit_then_a_small_call(moe):
+    # T*k = 4,194,304 pairs over 128 local experts: 2048 chunks x 128 = 262144
+    # entries, the whole array; then a small problem on a partial range
+    big = synth.config("prefill_full", T=1 << 19, H=64)
+    assert -(-big["T"] * big["k"] // 2048) * (big["e1"] - big["e0"]) == 1 << 18
+    r1 = _dispatch_both(moe, big)
+    r2 = _dispatch_both(moe, synth.config("tiny", e0=3, e1=11))
+    assert r1 == (1 << 19) * 8 and r2 > 0
 
 
 def test_noalloc_rejects_problems_beyond_its_fixed_scratch(moe):
