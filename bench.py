@@ -40,7 +40,7 @@ LOAD_SECONDS = 3.0  # back-to-back steps under the clock sampler, outside the ti
 L2_FLUSH_BYTES = 256 << 20
 _CS = "expert_routing_dispatch_gb300/csrc/"
 KERNEL_SOURCES = {
-    "grouped_gemm_gate_up": [_CS + "grouped_ffn.cu", _CS + "grouped_gemm.cuh", _CS + "common.cuh"],
+    "grouped_gemm_gate_up": [_CS + "grouped_ffn.cu", _CS + "grouped_gemm_pair.cuh", _CS + "common.cuh"],
     "grouped_ffn_mx": [_CS + "mxfp8.cu", _CS + "grouped_gemm_mx.cuh", _CS + "common.cuh"],
     "moe_layer_fused": [_CS + "decode_fused.cu", _CS + "grouped_gemm.cuh", _CS + "common.cuh", _CS + "route.cuh",
                         _CS + "combine.cuh"],
@@ -351,7 +351,7 @@ def run_ours(args):
     row_pair = torch.empty(P, dtype=i32, device=dev)
     pair_row = torch.empty(P, dtype=i32, device=dev)
     x_perm = torch.empty((P, H), dtype=torch.int16, device=dev)
-    h = torch.empty((P, I), dtype=torch.int16, device=dev)
+    h = torch.empty((P, 2 * I), dtype=torch.int16, device=dev)  # bf16 hi and lo terms of h
     y_perm = torch.empty((P, H), dtype=f32, device=dev)
     out = torch.empty((T, H), dtype=f32, device=dev)
     status = torch.zeros(1, dtype=i32, device=dev)

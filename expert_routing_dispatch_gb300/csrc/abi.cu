@@ -39,6 +39,46 @@ cudaError_t ensure_dynamic_smem(const void* func, int bytes) {
     return e;
 }
 
+cudaError_t max_active_clusters(const void* func, int cluster_size, int threads, int smem_bytes, int* clusters) {
+    constexpr int kSlots = 64;
+    static std::mutex mu;
+    static const void* seen_func[kSlots];
+    static int seen_dev[kSlots], seen_n[kSlots];
+    static int nseen = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < nseen; ++i)
+        if (seen_func[i] == func && seen_dev[i] == dev) {
+            *clusters = seen_n[i];
+            return cudaSuccess;
+        }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster_size);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = cluster_size;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, func, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    if (nseen < kSlots) {
+        seen_func[nseen] = func;
+        seen_dev[nseen] = dev;
+        seen_n[nseen] = n;
+        ++nseen;
+    }
+    *clusters = n;
+    return cudaSuccess;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;

@@ -26,6 +26,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// h carried as two bf16 terms: hi = bf16(v), lo = bf16(v - hi); hi + lo is v to
+// about 2^-17 relative.  Returns the packed hi pair and writes the packed lo pair.
+__device__ __forceinline__ uint32_t pack_bf16x2_hi_lo(float a, float b, uint32_t& lo) {
+    const uint32_t hi = pack_bf16x2(a, b);
+    lo = pack_bf16x2(a - bf16_lo(hi), b - bf16_hi(hi));  // both differences are exact in fp32
+    return hi;
+}
+// Column of h element `col` in the split layout [rows, 2 I]: each 64-column block
+// j of h becomes columns 128 j .. 128 j + 63 (hi) followed by 128 j + 64 .. 128 j + 127
+// (lo), so the down GEMM's k-blocks alternate hi and lo of the same weight k-block.
+__host__ __device__ __forceinline__ int h_hi_col(int col) { return col + (col & ~63); }
+
 // ------------------------------------------------------------------ smem
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

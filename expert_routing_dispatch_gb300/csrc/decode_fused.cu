@@ -11,9 +11,10 @@
 //                   pairs of its own token slice in pair order and copies their
 //                   x rows into x_perm
 //   --  barrier 2
-//   P2  gate/up     grouped tcgen05 GEMM + SiLU*up (grouped_gemm.cuh) -> h
+//   P2  gate/up     grouped tcgen05 GEMM + SiLU*up (grouped_gemm.cuh) -> h, as
+//                   bf16 hi + lo terms
 //   --  barrier 3
-//   P3  down        grouped tcgen05 GEMM -> y_perm
+//   P3  down        grouped tcgen05 GEMM over both terms -> y_perm
 //   --  barrier 4
 //   P4  combine     tokens striped over the CTAs (combine.cuh) -> out
 // Intermediates go through global memory; at decode sizes (T*k <= 8192 rows)
@@ -238,8 +239,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // ---------------- P2: gate/up GEMM + SiLU*up
     if (ok) {
-        const Args ga{a.h, a.status, n, a.H / BK, (a.I + a.bn / 2 - 1) / (a.bn / 2), a.I, a.I, a.bn / 2, 0, a.bn,
-                      SMALL_ROWS};
+        const Args ga{a.h, a.status, n, a.H / BK, (a.I + a.bn / 2 - 1) / (a.bn / 2), a.I, a.I, a.bn / 2, a.bn,
+                      SMALL_ROWS, 0, 0};
         build_tile_table(c, n, ga.ntiles_n, ga.bn);
         __syncthreads();
         run_phase<MODE_GATEUP>(c, ring, p, &tmX, &wmGU, ga, &tmXs);
@@ -248,8 +249,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // ---------------- P3: down GEMM
     if (ok) {
-        // no weight prefetch here: measured slower in this launch
-        const Args da{a.y_perm, a.status, n, a.I / BK, (a.H + a.bn - 1) / a.bn, a.H, a.H, a.bn, 0, a.bn, SMALL_ROWS};
+        // K = 2 I: h as hi and lo terms, each pair of k-blocks against one weight k-block
+        const Args da{a.y_perm, a.status, n, 2 * a.I / BK, (a.H + a.bn - 1) / a.bn, a.H, a.H, a.bn, a.bn, SMALL_ROWS,
+                      1, 0};
         build_tile_table(c, n, da.ntiles_n, da.bn);
         __syncthreads();
         run_phase<MODE_DOWN>(c, ring, p, &tmH, &wmD, da, &tmHs);
@@ -287,9 +289,9 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     const int bn = BN;
     CUtensorMap mX, mH, mXs, mHs;
     WMaps wGU, wD;
-    if (!make_tmap_bf16(&mXs, x_perm, rows, H, SMALL_ROWS) || !make_tmap_bf16(&mHs, h, rows, I, SMALL_ROWS) ||
+    if (!make_tmap_bf16(&mXs, x_perm, rows, H, SMALL_ROWS) || !make_tmap_bf16(&mHs, h, rows, 2 * I, SMALL_ROWS) ||
         !make_tmap_bf16(&mX, x_perm, rows, H, BM) || !make_wmaps(&wGU, w_gate, w_up, (long long)n * I, H, bn / 2) ||
-        !make_tmap_bf16(&mH, h, rows, I, BM) || !make_wmaps(&wD, w_down, nullptr, (long long)n * H, I, bn))
+        !make_tmap_bf16(&mH, h, rows, 2 * I, BM) || !make_wmaps(&wD, w_down, nullptr, (long long)n * H, I, bn))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
     if (e != cudaSuccess) return e;

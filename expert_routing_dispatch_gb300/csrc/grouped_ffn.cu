@@ -3,11 +3,14 @@
 // Two persistent launches over the grouped rows made by dispatch (the prefill
 // path of "Hosting Qwen on Blackwell", section "Expert Parallel": the prefill
 // layer is split into several kernels): the gate/up GEMM with the SiLU*up
-// epilogue writes h (bf16), the down GEMM writes y_perm (fp32).  The tile
-// loop, the TMA/tcgen05 pipeline and the epilogues live in grouped_gemm.cuh.
+// epilogue writes h as two bf16 terms (hi + lo, split layout [rows, 2 I]), the
+// down GEMM writes y_perm (fp32) from both terms.  The tile loop, the TMA/tcgen05
+// pipeline on CTA pairs and the epilogues live in grouped_gemm_pair.cuh.  This
+// file also builds the TMA descriptors that the fused decode kernel uses.
 #include <mutex>
 
 #include "grouped_gemm.cuh"
+#include "grouped_gemm_pair.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -15,49 +18,37 @@ namespace moe {
 namespace {
 
 using namespace gemm;
-static_assert(SMEM_BYTES <= 232448, "grouped GEMM exceeds the 227 KB shared-memory limit");
 
-// L2 prefetch of weight boxes by the first m-tile of each weight tile (k-blocks
-// ahead; GB300 measurements: down -5% at 6000 tokens and -6% at 16384 with 8,
-// gate/up within noise; the fused decode launch is faster without it)
-constexpr int kPrefetchGateUp = 0;
-constexpr int kPrefetchDown = 8;
+static_assert(pair::SMEM_BYTES <= 232448, "CTA-pair GEMM exceeds the 227 KB shared-memory limit");
 
-struct FfnArgs {
-    const int32_t* offsets;
-    Args g;
-};
-
+// The split path's GEMMs: one tile stream over CTA pairs (grouped_gemm_pair.cuh).
 template <int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ WMaps wm,
-                       const FfnArgs args) {
+__global__ void __launch_bounds__(pair::NUM_THREADS, 1)
+    grouped_ffn_pair_kernel(const __grid_constant__ pair::Maps maps, const int32_t* __restrict__ offsets,
+                            const pair::Args args) {
     extern __shared__ uint8_t smem_raw[];
-    const uint32_t ring = ring_base(smem_raw);
-    Ctl& c = ctl_of(smem_raw);
-    const int n = args.g.n;
+    const uint32_t ring = pair::ring_base(smem_raw);
+    pair::Ctl& c = pair::ctl_of(smem_raw);
+    const int n = args.n;
 
-    init(c, args.g.stall);
+    pair::init(c, args.stall);
     if (threadIdx.x == 0) {
-        tma_prefetch_desc(&tmA);
-        for (int i = 0; i < 3; ++i) {
-            tma_prefetch_desc(&wm.b0[i]);
-            if (MODE == MODE_GATEUP) tma_prefetch_desc(&wm.b1[i]);
-        }
+        tma_prefetch_desc(&maps.w0);
+        if (MODE == pair::MODE_GATEUP) tma_prefetch_desc(&maps.w1);
+        for (int i = 0; i < pair::TOKEN_BOXES; ++i) tma_prefetch_desc(&maps.tok[i]);
     }
-    for (int i = threadIdx.x; i <= n; i += NUM_THREADS) c.row_off[i] = __ldg(args.offsets + i);
+    for (int i = threadIdx.x; i <= n; i += pair::NUM_THREADS) c.row_off[i] = __ldg(offsets + i);
     __syncthreads();
-    build_tile_table(c, n, args.g.ntiles_n, args.g.bn);
+    pair::build_tile_table(c, n, args.nwb);
     tc_fence_before();
     __syncthreads();
+    pair::cluster_sync();  // both CTAs' barriers exist before any copy or arrive crosses over
     tc_fence_after();
 
-    Pipe p;
-    pipe_reset(p);
-    run_phase<MODE>(c, ring, p, &tmA, &wm, args.g);
+    pair::run<MODE>(c, ring, &maps, args);
 
     __syncthreads();
-    teardown(c, p, args.g.status);
+    pair::teardown(c, args.status);
 }
 
 }  // namespace
@@ -107,41 +98,63 @@ bool make_wmaps(WMaps* m, const void* w0, const void* w1, long long total_rows, 
 
 namespace {
 
+// Launch a CTA-pair GEMM: as many pairs as fit on the device at once, one tile
+// stream over them.
 template <int MODE>
-cudaError_t set_smem_attr() {
-    return ensure_dynamic_smem(reinterpret_cast<const void*>(&grouped_ffn_kernel<MODE>), (int)SMEM_BYTES);
+cudaError_t launch_pair(const pair::Maps& maps, const int32_t* offsets, const pair::Args& args, cudaStream_t s) {
+    const void* fn = reinterpret_cast<const void*>(&grouped_ffn_pair_kernel<MODE>);
+    cudaError_t e = ensure_dynamic_smem(fn, (int)pair::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    int clusters = 0;
+    if ((e = max_active_clusters(fn, 2, pair::NUM_THREADS, (int)pair::SMEM_BYTES, &clusters)) != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(pair::NUM_THREADS);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, grouped_ffn_pair_kernel<MODE>, maps, offsets, args);
+}
+
+// token maps of the pair GEMMs: boxes of 16, 32, ..., 128 rows
+bool make_token_maps(pair::Maps* m, const void* tokens, long long rows, int cols) {
+    for (int i = 0; i < pair::TOKEN_BOXES; ++i)
+        if (!make_tmap_bf16(&m->tok[i], tokens, rows, cols, 16 * (i + 1))) return false;
+    return true;
 }
 
 }  // namespace
 
-size_t ffn_scratch_bytes(long long rows, int I) { return (size_t)rows * (size_t)I * 2; }
+// h as hi and lo bf16 terms: [rows, 2 I]
+size_t ffn_scratch_bytes(long long rows, int I) { return (size_t)rows * (size_t)I * 4; }
 
 cudaError_t launch_gate_up(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
                            const uint16_t* w_up, uint16_t* h, long long rows, int H, int I, int n, int32_t* status,
                            cudaStream_t s, int stall) {
-    cudaError_t e;
-    if ((e = set_smem_attr<MODE_GATEUP>()) != cudaSuccess) return e;
-    CUtensorMap mA;
-    WMaps wm;
-    if (!make_tmap_bf16(&mA, x_perm, rows, H, BM) || !make_wmaps(&wm, w_gate, w_up, (long long)n * I, H, BN / 2))
+    pair::Maps maps;
+    if (!make_token_maps(&maps, x_perm, rows, H) || !make_tmap_bf16(&maps.w0, w_gate, (long long)n * I, H, 64) ||
+        !make_tmap_bf16(&maps.w1, w_up, (long long)n * I, H, 64))
         return cudaErrorInvalidValue;
-    FfnArgs a{offsets,
-              {h, status, n, H / BK, (I + BN / 2 - 1) / (BN / 2), I, I, BN / 2, kPrefetchGateUp, BN, 0, stall}};
-    grouped_ffn_kernel<MODE_GATEUP><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mA, wm, a);
-    return cudaGetLastError();
+    const pair::Args a{h, status, n, H / pair::BK, (I + 127) / 128, I, I, 0, stall};
+    return launch_pair<pair::MODE_GATEUP>(maps, offsets, a, s);
 }
 
 cudaError_t launch_down(const uint16_t* h, const int32_t* offsets, const uint16_t* w_down, float* y_perm,
                         long long rows, int H, int I, int n, int32_t* status, cudaStream_t s) {
-    cudaError_t e;
-    if ((e = set_smem_attr<MODE_DOWN>()) != cudaSuccess) return e;
-    CUtensorMap mH;
-    WMaps wm;
-    if (!make_tmap_bf16(&mH, h, rows, I, BM) || !make_wmaps(&wm, w_down, nullptr, (long long)n * H, I, BN))
+    pair::Maps maps;
+    if (!make_token_maps(&maps, h, rows, 2 * I) || !make_tmap_bf16(&maps.w0, w_down, (long long)n * H, I, 128))
         return cudaErrorInvalidValue;
-    FfnArgs a{offsets, {y_perm, status, n, I / BK, (H + BN - 1) / BN, H, H, BN, kPrefetchDown, BN, 0}};
-    grouped_ffn_kernel<MODE_DOWN><<<sm_count(), NUM_THREADS, SMEM_BYTES, s>>>(mH, wm, a);
-    return cudaGetLastError();
+    maps.w1 = maps.w0;
+    // K = 2 I: the k-blocks alternate hi and lo of h against the same W_down k-block
+    const pair::Args a{y_perm, status, n, 2 * I / pair::BK, (H + 255) / 256, H, H, 1, 0};
+    return launch_pair<pair::MODE_DOWN>(maps, offsets, a, s);
 }
 
 cudaError_t launch_expert_ffn(const uint16_t* x_perm, const int32_t* offsets, const uint16_t* w_gate,
@@ -156,12 +169,13 @@ cudaError_t launch_expert_ffn(const uint16_t* x_perm, const int32_t* offsets, co
 }  // namespace moe
 
 #ifdef MOE_GEMM_PROFILE
-// tuning builds only: reset / read the role wait counters of grouped_gemm.cuh
-extern "C" int moe_debug_gemm_prof(unsigned long long* host8, int reset) {
-    cudaError_t e = cudaMemcpyFromSymbol(host8, moe::gemm::g_gemm_prof, sizeof(unsigned long long) * 8);
+// tuning builds only: reset / read the role wait counters of grouped_gemm_pair.cuh
+// ([0..7] gate/up, [8..15] down)
+extern "C" int moe_debug_gemm_prof(unsigned long long* host16, int reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(host16, moe::pair::g_pair_prof, sizeof(unsigned long long) * 16);
     if (reset) {
-        unsigned long long z[8] = {};
-        e = cudaMemcpyToSymbol(moe::gemm::g_gemm_prof, z, sizeof(z));
+        unsigned long long z[16] = {};
+        e = cudaMemcpyToSymbol(moe::pair::g_pair_prof, z, sizeof(z));
     }
     return e == cudaSuccess ? 0 : 4;
 }

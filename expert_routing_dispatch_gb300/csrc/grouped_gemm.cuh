@@ -1,15 +1,18 @@
-// grouped_gemm.cuh -- device core of the grouped expert GEMMs on the tcgen05
-// tensor cores, shared by the split kernels (grouped_ffn.cu) and the fused
-// decode kernel (decode_fused.cu).
+// grouped_gemm.cuh -- device core of the one-CTA grouped expert GEMMs on the
+// tcgen05 tensor cores, used by the fused decode kernel (decode_fused.cu).  The
+// split prefill path runs the CTA-pair core of grouped_gemm_pair.cuh instead.
 //
 // "Hosting Qwen on Blackwell", section "MoE GEMM": the expert FFN is a grouped
-// GEMM over the experts, dense at prefill (~375 rows per expert, "Prefillers")
-// and bound by streaming the weights from HBM at decode ("Decoders").
+// GEMM over the experts, bound by streaming the weights from HBM at decode
+// ("Decoders").
 //
 // Two phases over the grouped rows made by dispatch:
 //   gate/up : acc[128 x 256] = x_perm[rows] . [W_gate[e] rows n..n+127 ; W_up[e] rows n..n+127]^T
-//             epilogue h = bf16(silu(acc[:, 0:128]) * acc[:, 128:256])   (fp32 math)
-//   down    : acc[128 x 256] = h[rows] . W_down[e][n..n+255]^T  ->  y_perm = acc (fp32)
+//             epilogue h = silu(acc[:, 0:128]) * acc[:, 128:256] (fp32 math), stored
+//             as two bf16 terms hi + lo in the split layout [rows, 2 I] (common.cuh)
+//   down    : acc[128 x 256] = h[rows] . W_down[e][n..n+255]^T over K = 2 I: the
+//             k-blocks alternate hi and lo of h against the same weight k-block,
+//             so y_perm = W_down (hi + lo) (fp32)
 // Tiles are (expert, m-tile of 128 rows, n-tile); the tile table is built on
 // the device from the row offsets.  Within an expert the m-tiles of one n-tile
 // are consecutive, so CTAs running side by side share a weight tile through L2.
@@ -31,23 +34,8 @@
 namespace moe {
 namespace gemm {
 
-// Tile shape.  BK = 64 bf16 (128-byte rows, 128-byte swizzle) with 4 stages is the
-// default; BK = 32 (64-byte rows, 64-byte swizzle) with 8 stages keeps the same
-// ring bytes with finer refill granularity.
-#ifndef MOE_GEMM_BK
-#define MOE_GEMM_BK 64
-#endif
-#ifndef MOE_GEMM_STAGES
-#define MOE_GEMM_STAGES (256 / MOE_GEMM_BK * 1)
-#endif
-#ifndef MOE_GEMM_B_POLICY
-// weights' L2 policy: 0 evict_first, 1 evict_last, 2 evict_normal.  evict_last
-// measured best on GB300: a weight tile is read by every m-tile of its expert
-// (gate/up 1580 vs 1462 TFLOP/s on the 16384-token workload, 1126 vs 1099 at 6000)
-#define MOE_GEMM_B_POLICY 1
-#endif
-constexpr int BM = 128, BN = 256, BK = MOE_GEMM_BK, STAGES = MOE_GEMM_STAGES;
-static_assert(BK == 64 || BK == 32, "BK must be 64 (128-byte swizzle) or 32 (64-byte swizzle)");
+// Tile shape: BK = 64 bf16 (128-byte rows, 128-byte swizzle), 4 ring stages.
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int ROW_BYTES = BK * 2;  // bytes of one K-row of a tile = swizzle span
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
@@ -58,23 +46,6 @@ constexpr int MAX_LOCAL = 1024;
 constexpr long long WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
-
-#ifdef MOE_GEMM_PROFILE
-// Tuning builds only: clock cycles each role spends waiting, summed over CTAs.
-// [0] producer waits on a free stage   [1] producer total
-// [2] MMA waits on a free accumulator  [3] MMA waits on loaded data  [4] MMA total
-// [5] epilogue waits on an accumulator (per warp)  [6] epilogue total (per warp)  [7] tiles
-__device__ unsigned long long g_gemm_prof[8];
-#define MOE_PROF_WAIT(acc, call)                \
-    ([&]() {                                    \
-        const long long _t = clock64();         \
-        const bool _r = (call);                 \
-        acc += clock64() - _t;                  \
-        return _r;                              \
-    }())
-#else
-#define MOE_PROF_WAIT(acc, call) (call)
-#endif
 
 struct Ctl {
     // per epilogue warp: a 32-row x 128-byte staging tile (16-byte slots XOR-swizzled by
@@ -96,17 +67,17 @@ struct Ctl {
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
 
 struct Args {
-    void* out;        // h bf16 (gate/up) or y_perm fp32 (down), row-major [rows, out_cols]
+    void* out;        // h bf16 [rows, 2 I] (gate/up, split hi/lo layout) or y_perm fp32 [rows, H] (down)
     int32_t* status;  // device status word or NULL
     int n;            // local experts
-    int kblocks;      // K / 64
+    int kblocks;      // k-blocks of the token operand: H / 64 (gate/up) or 2 I / 64 (down)
     int ntiles_n;     // n-tiles per expert
     int out_cols;     // I (gate/up) or H (down)
     int b_rows;       // weight rows per expert in the B tensor map (I or H)
     int n_step;       // output columns per n-tile (bn / 2 for gate/up, bn for down)
-    int prefetch;     // L2 prefetch distance of the weight boxes in k-blocks (0 = off)
     int bn;           // MMA N = weight rows per tile (256; 128 also supported)
     int a_small;      // box rows of the optional small token map (0 = none)
+    int ksplit;       // weight k-block of token k-block kb: kb >> ksplit (1 for down: hi and lo share it)
     int stall;        // testing hook: extra arrivals ring stage 0 waits for (0 in normal use)
 };
 
@@ -239,148 +210,93 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
 
     if (warp == 0) {
         // ================= TMA producer: the whole warp loops, the elected lane issues =================
-        {
-            long long w_empty = 0, t_begin = clock64();
-            (void)w_empty;
-            (void)t_begin;
-#if defined(MOE_GEMM_A_POLICY) && MOE_GEMM_A_POLICY == 0
-            const uint64_t pol_a = l2_policy_evict_first();
-#elif defined(MOE_GEMM_A_POLICY) && MOE_GEMM_A_POLICY == 2
-            const uint64_t pol_a = l2_policy_evict_normal();
-#else
-            const uint64_t pol_a = l2_policy_evict_last();  // token rows are reread for every n-tile
-#endif
-#if MOE_GEMM_B_POLICY == 0
-            const uint64_t pol_b = l2_policy_evict_first();
-#elif MOE_GEMM_B_POLICY == 1
-            const uint64_t pol_b = l2_policy_evict_last();
-#else
-            const uint64_t pol_b = l2_policy_evict_normal();
-#endif
-            int e_hint = 0;
-            TileCoord tc;
-            bool ok = !__any_sync(0xffffffffu, *abort_flag);
-            for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
-                const int a_row = c.row_off[tc.e] + tc.mt * BM;
-                const int piece_rows = args.n_step >> tc.shift;  // weight rows of one map's box
-                const int b_row = tc.e * args.b_rows + tc.nt * args.n_step + tc.piece * piece_rows;
-                const int bn_t = args.bn >> tc.shift;
-                const CUtensorMap* tmB0 = &wm->b0[tc.shift];
-                const CUtensorMap* tmB1 = &wm->b1[tc.shift];
-                const bool a_small = tmA_small != nullptr && tc.cnt - tc.mt * BM <= args.a_small;
-                const CUtensorMap* tma_a = a_small ? tmA_small : tmA;
-                const uint32_t stage_tx = (uint32_t)((a_small ? args.a_small : BM) * BK * 2 + bn_t * BK * 2);
-                for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
-                    const int s = p.g % STAGES, r = p.g / STAGES;
-                    if (!__all_sync(0xffffffffu,
-                                    MOE_PROF_WAIT(w_empty, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1,
-                                                                             abort_flag, args.status, WAIT_LIMIT)))) {
-                        ok = false;
-                        break;
-                    }
-                    p.issued[s] = r + 1;
-                    if (elect_one()) {
-                        // The first m-tile of each weight tile pulls the weight boxes PF k-blocks
-                        // ahead into L2 (only boxes wholly inside the tensor).
-                        const int PF = args.prefetch;
-                        if (PF > 0 && tc.shift == 0 && tc.mt == 0 && kb + PF < args.kblocks &&
-                            b_row + (MODE == MODE_GATEUP ? args.bn / 2 : args.bn) <= n * args.b_rows) {
-                            tma_prefetch_l2_2d(tmB0, (kb + PF) * BK, b_row);
-                            if (MODE == MODE_GATEUP) tma_prefetch_l2_2d(tmB1, (kb + PF) * BK, b_row);
-                        }
-                        // Each copy takes ~100 cycles to issue.  Gate/up issues its two weight
-                        // boxes before the token box (measured: -1% EP rank, -2% at 16384 tokens);
-                        // down keeps the token box first (the other order was 3-5% slower).
-                        const uint32_t fb = smem_u32(&c.full[s]);
-                        mbar_arrive_expect_tx(fb, stage_tx);
-                        if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn_t/2 each
-                            tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
-                            tma_load_2d(b_addr(s) + (uint32_t)(bn_t / 2) * BK * 2, tmB1, kb * BK, b_row, fb, pol_b);
-                            tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
-                        } else {
-                            tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
-                            tma_load_2d(b_addr(s), tmB0, kb * BK, b_row, fb, pol_b);
-                        }
-                    }
-                    __syncwarp();
+        const uint64_t pol_a = l2_policy_evict_last();  // token rows are reread for every n-tile
+        const uint64_t pol_b = l2_policy_evict_last();  // a weight tile is read by every m-tile of its expert
+        int e_hint = 0;
+        TileCoord tc;
+        bool ok = !__any_sync(0xffffffffu, *abort_flag);
+        for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
+            const int a_row = c.row_off[tc.e] + tc.mt * BM;
+            const int piece_rows = args.n_step >> tc.shift;  // weight rows of one map's box
+            const int b_row = tc.e * args.b_rows + tc.nt * args.n_step + tc.piece * piece_rows;
+            const int bn_t = args.bn >> tc.shift;
+            const CUtensorMap* tmB0 = &wm->b0[tc.shift];
+            const CUtensorMap* tmB1 = &wm->b1[tc.shift];
+            const bool a_small = tmA_small != nullptr && tc.cnt - tc.mt * BM <= args.a_small;
+            const CUtensorMap* tma_a = a_small ? tmA_small : tmA;
+            const uint32_t stage_tx = (uint32_t)((a_small ? args.a_small : BM) * BK * 2 + bn_t * BK * 2);
+            for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
+                const int s = p.g % STAGES, r = p.g / STAGES;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
+                                                               args.status, WAIT_LIMIT))) {
+                    ok = false;
+                    break;
                 }
+                p.issued[s] = r + 1;
+                if (elect_one()) {
+                    // Each copy takes ~100 cycles to issue.  Gate/up issues its two weight
+                    // boxes before the token box; down keeps the token box first.
+                    const uint32_t fb = smem_u32(&c.full[s]);
+                    const int wk = (kb >> args.ksplit) * BK;
+                    mbar_arrive_expect_tx(fb, stage_tx);
+                    if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn_t/2 each
+                        tma_load_2d(b_addr(s), tmB0, wk, b_row, fb, pol_b);
+                        tma_load_2d(b_addr(s) + (uint32_t)(bn_t / 2) * BK * 2, tmB1, wk, b_row, fb, pol_b);
+                        tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
+                    } else {
+                        tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
+                        tma_load_2d(b_addr(s), tmB0, wk, b_row, fb, pol_b);
+                    }
+                }
+                __syncwarp();
             }
-#ifdef MOE_GEMM_PROFILE
-            if (lane == 0) {
-                atomicAdd(&g_gemm_prof[0], (unsigned long long)w_empty);
-                atomicAdd(&g_gemm_prof[1], (unsigned long long)(clock64() - t_begin));
-            }
-#endif
         }
     } else if (warp == 1) {
         // ================= MMA issuer: the whole warp loops, the elected lane issues =================
         // (every branch is warp-uniform, so elect_one() always picks the same lane)
-        {
-            long long w_acc = 0, w_full = 0, t_begin = clock64(), ntiles = 0;
-            (void)w_acc;
-            (void)w_full;
-            (void)t_begin;
-            (void)ntiles;
-            int e_hint = 0;
-            TileCoord tc;
-            bool ok = !__any_sync(0xffffffffu, *abort_flag);
-            const uint64_t a_desc0 = sdesc_k_swz<ROW_BYTES>(a_addr(0)), b_desc0 = sdesc_k_swz<ROW_BYTES>(b_addr(0));
-            for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++p.it) {
-                const int acc = p.it & 1, use = p.it >> 1;
-                ++ntiles;
-                if (!__all_sync(0xffffffffu, MOE_PROF_WAIT(w_acc, mbar_wait_bounded(smem_u32(&c.tempty[acc]),
-                                                                                   (use & 1) ^ 1, abort_flag,
-                                                                                   args.status, WAIT_LIMIT))))
+        int e_hint = 0;
+        TileCoord tc;
+        bool ok = !__any_sync(0xffffffffu, *abort_flag);
+        const uint64_t a_desc0 = sdesc_k_swz<ROW_BYTES>(a_addr(0)), b_desc0 = sdesc_k_swz<ROW_BYTES>(b_addr(0));
+        for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++p.it) {
+            const int acc = p.it & 1, use = p.it >> 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1, abort_flag,
+                                                           args.status, WAIT_LIMIT)))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * BN);
+            const uint32_t idesc = idesc_bf16_f32(BM, args.bn >> tc.shift);
+            for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
+                const int s = p.g % STAGES, r = p.g / STAGES;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1, abort_flag, args.status,
+                                                               WAIT_LIMIT))) {
+                    ok = false;
                     break;
-                tc_fence_after();
-                const uint32_t d_tmem = c.tmem_base + (uint32_t)(acc * BN);
-                const uint32_t idesc = idesc_bf16_f32(BM, args.bn >> tc.shift);
-                for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
-                    const int s = p.g % STAGES, r = p.g / STAGES;
-                    if (!__all_sync(0xffffffffu, MOE_PROF_WAIT(w_full, mbar_wait_bounded(smem_u32(&c.full[s]), r & 1,
-                                                                                       abort_flag, args.status,
-                                                                                       WAIT_LIMIT)))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        // descriptors are linear in the address (bits 0-13 hold address >> 4)
-                        const uint64_t ad = a_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
-                        const uint64_t bd = b_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
-                            tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-                        tc_commit(smem_u32(&c.empty[s]));
-                    }
-                    __syncwarp();
                 }
-                if (!ok) break;
-                if (elect_one()) tc_commit(smem_u32(&c.tfull[acc]));
+                tc_fence_after();
+                if (elect_one()) {
+                    // descriptors are linear in the address (bits 0-13 hold address >> 4)
+                    const uint64_t ad = a_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
+                    const uint64_t bd = b_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
+                        tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    tc_commit(smem_u32(&c.empty[s]));
+                }
                 __syncwarp();
             }
-#ifdef MOE_GEMM_PROFILE
-            if (lane == 0) {
-                atomicAdd(&g_gemm_prof[2], (unsigned long long)w_acc);
-                atomicAdd(&g_gemm_prof[3], (unsigned long long)w_full);
-                atomicAdd(&g_gemm_prof[4], (unsigned long long)(clock64() - t_begin));
-                atomicAdd(&g_gemm_prof[7], (unsigned long long)ntiles);
-            }
-#endif
+            if (!ok) break;
+            if (elect_one()) tc_commit(smem_u32(&c.tfull[acc]));
+            __syncwarp();
         }
     } else {
         // ================= epilogue (warps 2..5, TMEM lane quarter = warp % 4) =================
         const int q = warp & 3;
-        long long w_tf = 0, t_begin = clock64();
-        (void)w_tf;
-        (void)t_begin;
         int e_hint = 0;
         TileCoord tc;
         for (int tile = blockIdx.x; !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++p.it) {
             const int acc = p.it & 1, use = p.it >> 1;
-            if (!MOE_PROF_WAIT(w_tf, mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status,
-                                                       WAIT_LIMIT)))
-                break;
+            if (!mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status, WAIT_LIMIT)) break;
             tc_fence_after();
             const int row0_in_e = tc.mt * BM + q * 32;  // first row of this warp's block
             const long long grow0 = (long long)c.row_off[tc.e] + row0_in_e;
@@ -389,8 +305,10 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             const int col0 = tc.nt * args.n_step + tc.piece * (args.n_step >> tc.shift);
             uint4* st = c.stage[q];
             if (MODE == MODE_GATEUP) {
-                // 32 h columns per chunk: 64 B per row, 4 slots; slot = piece ^ ((row >> 1) & 3)
+                // 32 h columns per chunk (one half of a 64-column block of the split layout):
+                // 64 B of hi and 64 B of lo per row, each staged as 4 slots; slot = piece ^ ((row >> 1) & 3)
                 uint16_t* out = static_cast<uint16_t*>(args.out);
+                const long long ld = 2ll * args.out_cols;
 #pragma unroll 1
                 for (int cc = 0; cc < bn_t / 2; cc += 32) {
                     uint32_t g0[16], g1[16], u0[16], u1[16];
@@ -399,31 +317,38 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     tmem_ld16(taddr + bn_t / 2 + cc, u0);
                     tmem_ld16(taddr + bn_t / 2 + cc + 16, u1);
                     tmem_ld_wait();
-                    uint32_t pk[16];
+                    uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float a0 = __uint_as_float(g0[2 * i]), a1 = __uint_as_float(g0[2 * i + 1]);
                         const float b0 = __uint_as_float(u0[2 * i]), b1 = __uint_as_float(u0[2 * i + 1]);
-                        pk[i] = pack_bf16x2(silu(a0) * b0, silu(a1) * b1);
+                        hi[i] = pack_bf16x2_hi_lo(silu(a0) * b0, silu(a1) * b1, lo[i]);
                         const float c0 = __uint_as_float(g1[2 * i]), c1 = __uint_as_float(g1[2 * i + 1]);
                         const float d0 = __uint_as_float(u1[2 * i]), d1 = __uint_as_float(u1[2 * i + 1]);
-                        pk[8 + i] = pack_bf16x2(silu(c0) * d0, silu(c1) * d1);
+                        hi[8 + i] = pack_bf16x2_hi_lo(silu(c0) * d0, silu(c1) * d1, lo[8 + i]);
                     }
                     const int sw = (lane >> 1) & 3;
+                    const int hcol = h_hi_col(col0 + cc);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        st[lane * 4 + (j ^ sw)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                    __syncwarp();
-                    if (col0 + cc < args.out_cols) {
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t* pk = part ? lo : hi;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int r = i * 8 + (lane >> 2), piece = lane & 3;
-                            const uint4 v = st[r * 4 + (piece ^ ((r >> 1) & 3))];
-                            if (row0_in_e + r < tc.cnt)
-                                *reinterpret_cast<uint4*>(out + (grow0 + r) * args.out_cols + col0 + cc + 8 * piece) = v;
+                        for (int j = 0; j < 4; ++j)
+                            st[lane * 4 + (j ^ sw)] =
+                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        __syncwarp();
+                        if (col0 + cc < args.out_cols) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int r = i * 8 + (lane >> 2), piece = lane & 3;
+                                const uint4 v = st[r * 4 + (piece ^ ((r >> 1) & 3))];
+                                if (row0_in_e + r < tc.cnt)
+                                    *reinterpret_cast<uint4*>(out + (grow0 + r) * ld + hcol + 64 * part + 8 * piece) =
+                                        v;
+                            }
                         }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
             } else {
                 // 32 fp32 columns per chunk: 128 B per row, 8 slots; slot = piece ^ (row & 7)
@@ -458,14 +383,8 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&c.tempty[acc]));
         }
-        // the stores above are read later through TMA (async proxy) by other CTAs
+        // the stores above are read later through TMA (async proxy)
         asm volatile("fence.proxy.async.global;" ::: "memory");
-#ifdef MOE_GEMM_PROFILE
-        if (lane == 0) {
-            atomicAdd(&g_gemm_prof[5], (unsigned long long)w_tf);
-            atomicAdd(&g_gemm_prof[6], (unsigned long long)(clock64() - t_begin));
-        }
-#endif
     }
 }
 

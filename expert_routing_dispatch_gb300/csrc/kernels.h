@@ -88,4 +88,9 @@ int sm_count();
 // of the kernel, so a process that drives several GPUs sets it on each of them.
 cudaError_t ensure_dynamic_smem(const void* func, int bytes);
 
+// Largest number of clusters of `cluster_size` CTAs of `func` (threads, dynamic
+// shared memory as given) resident on the current device at once; queried once
+// per (kernel, device).
+cudaError_t max_active_clusters(const void* func, int cluster_size, int threads, int smem_bytes, int* clusters);
+
 }  // namespace moe

@@ -136,14 +136,18 @@ int moe_dispatch_noalloc(const moe_dims* d, const uint16_t* x, const int32_t* to
 /*
  * Grouped SwiGLU expert FFN ("MoE GEMM" section), on the grouped rows made by
  * moe_dispatch: for each local expert e and row r in [offsets[e], offsets[e+1]):
- *   h[r]      = bf16( silu(x_perm[r] . W_gate[e]^T) * (x_perm[r] . W_up[e]^T) )
- *   y_perm[r] = h[r] . W_down[e]^T                                  (fp32)
- * bf16 operands, fp32 accumulation on the tcgen05 tensor cores, SiLU*up in fp32,
- * h rounded to bf16 (it is the second GEMM's operand), y kept in fp32.
+ *   h[r]      = silu(x_perm[r] . W_gate[e]^T) * (x_perm[r] . W_up[e]^T)      (fp32)
+ *   y_perm[r] = h[r] . W_down[e]^T                                          (fp32)
+ * bf16 operands, fp32 accumulation on the tcgen05 tensor cores, SiLU*up in fp32.
+ * h is the second GEMM's operand, which the bf16 tensor cores take as bf16: it is
+ * carried as two bf16 terms, hi = bf16(h) and lo = bf16(h - hi) (hi + lo equals h
+ * to about 2^-17), and the down GEMM runs over both (K = 2 I); y is kept in fp32.
+ * The split layout of h is [T*k, 2 I]: each 64-column block j of h becomes
+ * columns 128 j .. 128 j + 63 (hi) followed by 128 j + 64 .. 128 j + 127 (lo).
  *   x_perm   bf16 [T*k, H]; offsets int32 [n+1] (device, read by the kernels)
  *   w_gate, w_up  bf16 [n, I, H]; w_down bf16 [n, H, I]
  *   y_perm   fp32 [T*k, H] out (rows >= R are left untouched)
- *   ws       >= moe_expert_ffn_workspace_size(d) bytes (holds h)
+ *   ws       >= moe_expert_ffn_workspace_size(d) bytes (holds h, T*k * 2 I bf16)
  *   status_dev as in moe_route (MOE_ERR_TIMEOUT if an internal wait ran out)
  */
 int moe_expert_ffn(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets,
@@ -153,9 +157,10 @@ int moe_expert_ffn(const moe_dims* d, const uint16_t* x_perm, const int32_t* off
 /*
  * The two halves of moe_expert_ffn, for callers that keep h themselves (or
  * time the GEMMs apart).  Same row grouping, operands and rounding.
- *   moe_expert_gate_up: h[r] = bf16( silu(x_perm[r] . W_gate[e]^T) * (x_perm[r] . W_up[e]^T) )
- *                       h bf16 [T*k, I] out (rows >= R untouched)
- *   moe_expert_down:    y_perm[r] = h[r] . W_down[e]^T,  y_perm fp32 [T*k, H] out
+ *   moe_expert_gate_up: h[r] = silu(x_perm[r] . W_gate[e]^T) * (x_perm[r] . W_up[e]^T) as bf16
+ *                       hi + lo terms, h bf16 [T*k, 2 I] out in the split layout
+ *                       above (rows >= R untouched)
+ *   moe_expert_down:    y_perm[r] = (hi[r] + lo[r]) . W_down[e]^T,  y_perm fp32 [T*k, H] out
  */
 int moe_expert_gate_up(const moe_dims* d, const uint16_t* x_perm, const int32_t* offsets,
                        const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,

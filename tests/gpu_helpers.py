@@ -123,3 +123,70 @@ def rel_err(got, ref):
     rms = float(np.sqrt(np.mean(np.asarray(ref, np.float64) ** 2)))
     err = float(np.abs(np.asarray(got, np.float64) - ref).max()) if np.size(ref) else 0.0
     return err, rms
+
+
+# ---------------------------------------------------------------- MXFP8 rounding ambiguity
+_E4M3 = []
+
+
+def e4m3_magnitudes():
+    """The non-negative finite E4M3 values in code order (codes 0..126, ascending),
+    read from the oracle's dequantiser at block scale 2^0."""
+    if not _E4M3:
+        q = np.zeros((1, 128), np.uint8)
+        q[0, :127] = np.arange(127)
+        s = np.full((1, 4), 127, np.uint8)
+        _E4M3.append(oracle.mxfp8_dequantize(q, s)[0, :127])
+    return _E4M3[0]
+
+
+def mx_ambiguity(h64, hs, rel_tau=2.0 ** -10, abs_tau=2.0 ** -16, scale_tau=2.0 ** -14):
+    """Which E4M3 codes of the MXFP8 quantisation of h64 (fp64 [rows, I]; the
+    oracle's block scale codes hs [rows, I/32]) a kernel that computes h in fp32,
+    with another summation order, may legitimately round the other way.
+
+    An element is ambiguous when its scaled value v = |h| / X lies within
+    max(rel_tau * step, abs_tau * block max) of the rounding midpoint between its
+    two neighbouring E4M3 values (step = their spacing): there the fp32 value can
+    fall on either side.  A block is scale-ambiguous when its largest |h| lies
+    within a relative scale_tau of a power of two (the UE8M0 scale can then differ
+    by one), and all its elements count as ambiguous.  Returns (amb [rows, I],
+    delta [rows, I]: the most an ambiguous element's dequantised value can differ
+    from the oracle's, scale_amb [rows, I/32])."""
+    grid = e4m3_magnitudes()
+    rows, I = h64.shape
+    X = 2.0 ** (np.repeat(hs.astype(np.float64), 32, axis=1) - 127)
+    v = np.abs(h64) / X
+    j = np.clip(np.searchsorted(grid, v, side="left"), 1, grid.size - 1)
+    a, b = grid[j - 1], grid[j]
+    step = b - a
+    dist = np.abs(v - 0.5 * (a + b))
+    vmax = np.repeat(v.reshape(rows, I // 32, 32).max(axis=2), 32, axis=1)
+    amb = dist <= np.maximum(rel_tau * step, abs_tau * vmax)
+    delta = step * X
+    amax = np.abs(h64).reshape(rows, I // 32, 32).max(axis=2)
+    with np.errstate(divide="ignore"):
+        lg = np.log2(np.where(amax > 0, amax, 1.0))
+    scale_amb = (amax > 0) & (np.abs(lg - np.round(lg)) * np.log(2.0) <= scale_tau)
+    if scale_amb.any():
+        sa = np.repeat(scale_amb, 32, axis=1)
+        # at half the scale the values double and the largest saturate at 448
+        extra = 2.0 * step * X + np.maximum(0.0, 2.0 * v - 448.0) * X / 2.0
+        amb = amb | sa
+        delta = np.where(sa, np.maximum(delta, extra), delta)
+    return amb, np.where(amb, delta, 0.0), scale_amb
+
+
+def mx_down_bound(rows, offsets, wd, dh):
+    """Elementwise bound on how far the down GEMM's output rows move when their h
+    rows move by at most dh (fp64 [len(rows), I]): |W_down[e]| |dh| per row, with
+    W_down the dequantised MXFP8 weights (q, s) of each row's expert."""
+    q, s = wd
+    e_of = np.searchsorted(np.asarray(offsets), rows, side="right") - 1
+    out = np.zeros((len(rows), q.shape[1]))
+    for e in np.unique(e_of):
+        sel = np.nonzero(e_of == e)[0]
+        if not dh[sel].any():
+            continue
+        out[sel] = dh[sel] @ np.abs(oracle.mxfp8_dequantize(q[e], s[e])).T
+    return out

@@ -44,7 +44,7 @@ def test_gate_up_wait_timeout_reports_status_and_context_survives(moe):
     P, R = T * k, d["R"]
     xp, off = dev(x_perm), dev(d["offsets"])
     wg, wu, wd = dev(inp["w_gate"]), dev(inp["w_up"]), dev(inp["w_down"])
-    h = torch.zeros((P, I), dtype=torch.int16, device="cuda")
+    h = torch.zeros((P, 2 * I), dtype=torch.int16, device="cuda")  # h as bf16 hi and lo terms
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
     t0 = time.time()
