@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(pair::NUM_THREADS, 1)
     }
     for (int i = threadIdx.x; i <= n; i += pair::NUM_THREADS) c.row_off[i] = __ldg(offsets + i);
     __syncthreads();
-    pair::build_tile_table(c, n, args.nwb);
+    pair::build_tile_table(c, n, args.nwb, (int)pair::cluster_count());
     tc_fence_before();
     __syncthreads();
     pair::cluster_sync();  // both CTAs' barriers exist before any copy or arrive crosses over

@@ -25,8 +25,9 @@
 // all four lane quadrants) and the four MMAs, in order in the tensor pipe;
 // warps 2..5 run the epilogue; warps 6..9 gather the scale words from global
 // memory into the shared-memory chunks of ring slot warp - 6 (each warp owns one
-// slot and loads its next stage's words right after publishing one, so the
-// loads have four stages of MMAs to land before the warp's next proxy fence).
+// slot and keeps the words of its next two stages in registers, loading the
+// second right after publishing one, so the loads have eight stages of MMAs to
+// land before they are needed).
 // Every wait is bounded.
 #pragma once
 
@@ -370,8 +371,12 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
         long long wsf = 0, tsf = clock64();
         (void)wsf;
         (void)tsf;
-        uint32_t w[10];
-        for (int g = j; load(g, w) && !*abort_flag; g += STAGES) {
+        // two items in flight: the words of this slot's next stage and of the one after
+        // it are loaded before the warp waits for the slot to free up
+        uint32_t w[10], wn[10];
+        bool have = load(j, w);
+        bool have_n = have && load(j + STAGES, wn);
+        for (int g = j; have && !*abort_flag; g += STAGES) {
             const int r = g / STAGES;
             // the copies of this slot's previous round have completed with its MMAs
             if (!MX_PROF_WAIT(wsf, mbar_wait_bounded(smem_u32(&c.empty[j]), (r & 1) ^ 1, abort_flag, args.status,
@@ -383,6 +388,10 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by tcgen05.cp (async proxy)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&c.full[j]));
+#pragma unroll
+            for (int i = 0; i < 10; ++i) w[i] = wn[i];
+            have = have_n;
+            if (have_n) have_n = load(g + 2 * STAGES, wn);
         }
         if (lane == 0) {
             MX_PROF_ADD(8, wsf);

@@ -25,9 +25,14 @@
 //             segment per store.
 //
 // Tiles are (expert, weight block wb, token tile tt) with tt fastest, so the
-// clusters working side by side share each weight block through L2.  Cluster c
-// takes stream positions k*G + c for even k and k*G + G-1-c for odd k (G
-// clusters), which alternates big and small token tiles between clusters.
+// pairs working side by side share each weight block through L2 (a block read by
+// two pairs at the same time comes from HBM once).  An expert's c rows are cut
+// into ceil(c / 256) token tiles of equal size (a multiple of 16; 375 rows give
+// 192 + 183), so the tiles of one expert cost the same.  Cluster c of G takes
+// stream positions k G + c for even k and k G + G-1-c for odd k, which evens out
+// the differences between experts.  When the last round is sparse (r tiles,
+// r <= G / 2), each of its tiles runs as up to 4 pieces along N on different
+// pairs, so the last round spreads over more SMs.
 //
 // Roles (6 warps per CTA): warp 0 issues the TMA loads of its CTA's halves into
 // a 6-stage ring, all completing on the even CTA's `full` barrier (.cta_group::2
@@ -54,7 +59,13 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * TN;
 constexpr int MAX_LOCAL = 1024;
 constexpr int TOKEN_BOXES = 8;               // token boxes of 16, 32, ..., 128 rows
+constexpr int MAX_TAIL = 256;                // most tiles of a last round that is split into pieces
+constexpr int MAX_PIECES = 4;                // pieces per tile of the split last round
 constexpr long long WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
+// Down GEMM stage layout: one W_down k-block with the hi and the lo token k-blocks
+// that use it (48 KB, 4 stages), instead of one token k-block per stage with the
+// weight k-block loaded for each (32 KB, 6 stages).
+constexpr bool DOWN_SHARED_W = true;
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
@@ -90,9 +101,11 @@ struct Ctl {
     uint64_t xbar[2][2];     // gate/up epilogue: both warps of a quarter pair wrote a chunk's halves (64 arrivals)
     uint32_t tmem_base;
     int abort_flag;
-    int tile_total;
     int tile_start[MAX_LOCAL + 1];  // exclusive prefix of tiles per expert
     int row_off[MAX_LOCAL + 1];     // grouped-row offsets of the local experts
+    int tail_first;                 // first tile of the split last round (= tiles when none)
+    int stream_len;                 // whole tiles before the last round + pieces of its tiles
+    int tail_start[MAX_TAIL + 1];   // exclusive prefix of pieces over the last round's tiles
 };
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
 
@@ -117,8 +130,11 @@ struct Maps {
 };
 
 struct Tile {
-    int e, wb, tt, cnt, ntok;  // expert, weight block, token tile, rows of the expert, tokens in the tile
+    int e, wb, tok0, cnt, ntok;  // expert, weight block, first token (within the expert), rows of the expert,
+                                 // tokens in the piece (<= 256)
 };
+
+
 
 // ------------------------------------------------------------------ cluster PTX
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -250,15 +266,47 @@ __device__ __forceinline__ void init(Ctl& c, int stall) {
     }
 }
 
-// warp 0: tile_start from row_off (already in shared memory)
-__device__ __forceinline__ void build_tile_table(Ctl& c, int n, int nwb) {
+// rows of token tile tt of an expert with cnt rows: [tt ts, min(cnt, (tt + 1) ts))
+// with ts = ceil(cnt / ntt) rounded up to 16, ntt = ceil(cnt / 256)
+__device__ __forceinline__ int token_tiles(int cnt) { return (cnt + TN - 1) / TN; }
+__device__ __forceinline__ int token_tile_size(int cnt) {
+    const int ntt = token_tiles(cnt);
+    return ntt ? (((cnt + ntt - 1) / ntt + 15) & ~15) : 0;
+}
+
+// whole tile `tile` of the stream -> expert, weight block, token range
+__device__ __forceinline__ void tile_coords(const Ctl& c, int tile, int& e_hint, Tile& t) {
+    int e = e_hint;
+    while (c.tile_start[e + 1] <= tile) ++e;  // tiles increase along a cluster's stream
+    e_hint = e;
+    const int cnt = c.row_off[e + 1] - c.row_off[e];
+    const int ntt = token_tiles(cnt), ts = token_tile_size(cnt);
+    const int local = tile - c.tile_start[e];
+    const int tt = local % ntt;
+    t.e = e;
+    t.wb = local / ntt;
+    t.cnt = cnt;
+    t.tok0 = tt * ts;
+    t.ntok = min(ts, cnt - t.tok0);
+}
+
+// pieces of a last-round tile with ntok tokens when the round holds r tiles
+__device__ __forceinline__ int tail_pieces(int ntok, int r, int G) {
+    int s = min(MAX_PIECES, G / r);
+    s = min(s, (ntok + 31) / 32);  // pieces of at least 32 tokens
+    return max(s, 1);
+}
+
+// warp 0: tile_start from row_off (already in shared memory), then the split of
+// a sparse last round.  Every CTA of the grid computes the same table.
+__device__ __forceinline__ void build_tile_table(Ctl& c, int n, int nwb, int G) {
     if ((threadIdx.x >> 5) != 0) return;
     const int lane = threadIdx.x & 31;
     int carry = 0;
     for (int b0 = 0; b0 < n; b0 += 32) {
         const int e = b0 + lane;
         int v = 0;
-        if (e < n) v = ((c.row_off[e + 1] - c.row_off[e] + TN - 1) / TN) * nwb;
+        if (e < n) v = token_tiles(c.row_off[e + 1] - c.row_off[e]) * nwb;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, v, o);
@@ -267,28 +315,59 @@ __device__ __forceinline__ void build_tile_table(Ctl& c, int n, int nwb) {
         if (e < n) c.tile_start[e + 1] = carry + v;
         carry += __shfl_sync(0xffffffffu, v, 31);
     }
+    if (lane == 0) c.tile_start[0] = 0;
+    __syncwarp();
+    const int total = carry, r = total % G;
+    const bool split = r > 0 && 2 * r <= G && r <= MAX_TAIL;
+    const int tail_first = split ? total - r : total;
+    int pieces = 0;
+    if (split) {
+        int e_hint = 0;
+        for (int b0 = 0; b0 < r; b0 += 32) {
+            const int i = b0 + lane;
+            int v = 0;
+            if (i < r) {
+                Tile t;
+                tile_coords(c, tail_first + i, e_hint, t);
+                v = tail_pieces(t.ntok, r, G);
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += y;
+            }
+            if (i < r) c.tail_start[i + 1] = pieces + v;
+            pieces += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
     if (lane == 0) {
-        c.tile_start[0] = 0;
-        c.tile_total = carry;
+        c.tail_start[0] = 0;
+        c.tail_first = tail_first;
+        c.stream_len = tail_first + pieces;
     }
 }
 
-// stream position of this cluster's k-th tile (alternating direction per round)
+// stream position of this cluster's k-th piece (alternating direction per round)
 __device__ __forceinline__ int tile_of(int k, int cid, int G) { return k * G + ((k & 1) ? G - 1 - cid : cid); }
 
-__device__ __forceinline__ bool next_tile(const Ctl& c, int tile, int& e_hint, Tile& t) {
-    if (tile >= c.tile_total) return false;
-    int e = e_hint;
-    while (c.tile_start[e + 1] <= tile) ++e;  // positions increase along a cluster's stream
-    e_hint = e;
-    const int cnt = c.row_off[e + 1] - c.row_off[e];
-    const int ntt = (cnt + TN - 1) / TN;
-    const int local = tile - c.tile_start[e];
-    t.e = e;
-    t.wb = local / ntt;
-    t.tt = local - t.wb * ntt;
-    t.cnt = cnt;
-    t.ntok = min(TN, cnt - t.tt * TN);
+// Stream position -> the piece to compute.  Positions increase along a cluster's
+// stream, so the hints only move forward.
+__device__ __forceinline__ bool next_tile(const Ctl& c, int pos, int& e_hint, int& tail_hint, Tile& t) {
+    if (pos >= c.stream_len) return false;
+    if (pos < c.tail_first) {
+        tile_coords(c, pos, e_hint, t);
+        return true;
+    }
+    const int q = pos - c.tail_first;
+    int i = tail_hint;
+    while (c.tail_start[i + 1] <= q) ++i;
+    tail_hint = i;
+    tile_coords(c, c.tail_first + i, e_hint, t);
+    const int s = c.tail_start[i + 1] - c.tail_start[i], p = q - c.tail_start[i];
+    const int ps = ((t.ntok + s - 1) / s + 15) & ~15;
+    const int lo = min(t.ntok, p * ps), hi = min(t.ntok, (p + 1) * ps);
+    t.tok0 += lo;
+    t.ntok = hi - lo;
     return true;
 }
 
@@ -304,9 +383,15 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
     const uint32_t rank = cluster_rank();
     const int cid = (int)cluster_id(), G = (int)cluster_count();
     volatile int* abort_flag = &c.abort_flag;
-    auto a_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES); };
-    auto b_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES + A_BYTES); };
-    int e_hint = 0;
+    // stage geometry: KSUB token k-blocks per weight k-block in each of NST stages of SB bytes
+    constexpr bool SHARED_W = MODE == MODE_DOWN && DOWN_SHARED_W;
+    constexpr int KSUB = SHARED_W ? 2 : 1;
+    constexpr int NST = SHARED_W ? 4 : STAGES;
+    constexpr int SB = A_BYTES + KSUB * B_BYTES;
+    static_assert(NST * SB <= STAGES * STAGE_BYTES && NST <= STAGES, "stage layout exceeds the ring");
+    const int nsteps = args.kblocks / KSUB;
+    auto a_addr = [&](int s) { return ring + (uint32_t)(s * SB); };
+    auto b_addr = [&](int s) { return ring + (uint32_t)(s * SB + A_BYTES); };
     Tile t;
 
     if (warp == 0) {
@@ -315,19 +400,21 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
         (void)w_empty;
         (void)t_begin;
         const uint64_t pol_w = l2_policy_evict_last();  // a weight block is read by every token tile of its expert
-        const uint64_t pol_t = l2_policy_evict_last();  // token rows are read by every weight block
+        const uint64_t pol_t = l2_policy_evict_last();  // token rows are read by every weight block of the expert
         const uint32_t full0 = map_to_rank(smem_u32(&c.full[0]), 0);
         int g = 0;
         bool ok = !__any_sync(0xffffffffu, *abort_flag);
-        for (int k = 0; ok && next_tile(c, tile_of(k, cid, G), e_hint, t); ++k) {
+        int e_hint = 0, tail_hint = 0;
+        for (int k = 0; ok && next_tile(c, tile_of(k, cid, G), e_hint, tail_hint, t); ++k) {
+            if (t.ntok <= 0) continue;  // an empty piece of the split last round: every role skips it
             const int N = tile_n(t), half = N >> 1;
             const int box = (half + 15) / 16 - 1;  // token box of 16 (box + 1) >= half rows
-            const int tok_row = c.row_off[t.e] + t.tt * TN + (int)rank * half;
+            const int tok_row = c.row_off[t.e] + t.tok0 + (int)rank * half;
             const int w_row = MODE == MODE_GATEUP ? t.e * args.w_rows + t.wb * 128 + (int)rank * 64
                                                   : t.e * args.w_rows + t.wb * 256 + (int)rank * 128;
-            const uint32_t stage_tx = 2u * (uint32_t)(A_BYTES + 16 * (box + 1) * BK * 2);
-            for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
-                const int s = g % STAGES, r = g / STAGES;
+            const uint32_t stage_tx = 2u * (uint32_t)(A_BYTES + KSUB * 16 * (box + 1) * BK * 2);
+            for (int kb = 0; kb < nsteps; ++kb, ++g) {
+                const int s = g % NST, r = g / NST;
                 if (!__all_sync(0xffffffffu,
                                 PAIR_PROF_WAIT(w_empty, wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
                                                                      args.status, WAIT_LIMIT)))) {
@@ -336,7 +423,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
                 }
                 if (elect_one()) {
                     const uint32_t fb = full0 + (uint32_t)(s * 8);
-                    const int wk = (kb >> args.ksplit) * BK;
+                    const int wk = (SHARED_W ? kb : kb >> args.ksplit) * BK;  // weight k-block of this stage
                     if (rank == 0) mbar_arrive_expect_tx(smem_u32(&c.full[s]), stage_tx);
                     if (MODE == MODE_GATEUP) {  // [64 gate rows | 64 up rows] of the same h columns
                         tma_load_2d_pair(a_addr(s), &maps->w0, wk, w_row, fb, pol_w);
@@ -344,7 +431,10 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
                     } else {
                         tma_load_2d_pair(a_addr(s), &maps->w0, wk, w_row, fb, pol_w);
                     }
-                    tma_load_2d_pair(b_addr(s), &maps->tok[box], kb * BK, tok_row, fb, pol_t);
+#pragma unroll
+                    for (int sub = 0; sub < KSUB; ++sub)  // down, shared W: hi then lo k-block of h
+                        tma_load_2d_pair(b_addr(s) + (uint32_t)(sub * B_BYTES), &maps->tok[box], (kb * KSUB + sub) * BK,
+                                         tok_row, fb, pol_t);
                 }
                 __syncwarp();
             }
@@ -365,8 +455,11 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
         const uint64_t a_desc0 = sdesc_k_swz<128>(a_addr(0)), b_desc0 = sdesc_k_swz<128>(b_addr(0));
         int g = 0;
         bool ok = !__any_sync(0xffffffffu, *abort_flag);
-        for (int k = 0; ok && next_tile(c, tile_of(k, cid, G), e_hint, t); ++k) {
-            const int acc = k & 1, use = k >> 1;
+        int e_hint = 0, tail_hint = 0, it = 0;
+        for (int k = 0; ok && next_tile(c, tile_of(k, cid, G), e_hint, tail_hint, t); ++k) {
+            if (t.ntok <= 0) continue;
+            const int acc = it & 1, use = it >> 1;
+            ++it;
             ++ntiles;
             if (!__all_sync(0xffffffffu, PAIR_PROF_WAIT(w_acc, wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1,
                                                                              abort_flag, args.status, WAIT_LIMIT))))
@@ -374,8 +467,8 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
             tc_fence_after();
             const uint32_t d_tmem = tmem + (uint32_t)(acc * TN);
             const uint32_t idesc = idesc_bf16_f32(2 * WROWS, tile_n(t));
-            for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
-                const int s = g % STAGES, r = g / STAGES;
+            for (int kb = 0; kb < nsteps; ++kb, ++g) {
+                const int s = g % NST, r = g / NST;
                 if (!__all_sync(0xffffffffu, PAIR_PROF_WAIT(w_full, wait_bounded(smem_u32(&c.full[s]), r & 1,
                                                                                   abort_flag, args.status,
                                                                                   WAIT_LIMIT)))) {
@@ -385,11 +478,14 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
                 tc_fence_after();
                 if (elect_one()) {
                     // descriptors are linear in the address (bits 0-13 hold address >> 4)
-                    const uint64_t ad = a_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
-                    const uint64_t bd = b_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
+                    const uint64_t ad = a_desc0 + (uint64_t)((s * SB) >> 4);
+                    const uint64_t bd = b_desc0 + (uint64_t)((s * SB) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
-                        mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    for (int sub = 0; sub < KSUB; ++sub)
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
+                            mma_bf16_pair(d_tmem, ad + 2 * kk, bd + (uint64_t)((sub * B_BYTES) >> 4) + 2 * kk, idesc,
+                                          (kb | kk | sub) != 0);
                     commit_pair(smem_u32(&c.empty[s]));
                 }
                 __syncwarp();
@@ -412,14 +508,17 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
         (void)t_begin;
         const uint32_t tempty0 = map_to_rank(smem_u32(&c.tempty[0]), 0);
         int chunk_seq = 0;  // chunks exchanged so far (the two warps of a pair count alike)
-        for (int k = 0; !*abort_flag && next_tile(c, tile_of(k, cid, G), e_hint, t); ++k) {
-            const int acc = k & 1, use = k >> 1;
+        int e_hint = 0, tail_hint = 0, it = 0;
+        for (int k = 0; !*abort_flag && next_tile(c, tile_of(k, cid, G), e_hint, tail_hint, t); ++k) {
+            if (t.ntok <= 0) continue;
+            const int acc = it & 1, use = it >> 1;
+            ++it;
             if (!PAIR_PROF_WAIT(w_tf, wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status,
                                                    WAIT_LIMIT)))
                 break;
             tc_fence_after();
             const int N = tile_n(t);
-            const int tok0 = t.tt * TN;  // token (within the expert) of accumulator column 0
+            const int tok0 = t.tok0;  // token (within the expert) of accumulator column 0
             const long long row0 = (long long)c.row_off[t.e] + tok0;
             const uint32_t taddr = c.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * TN);
             if (MODE == MODE_GATEUP) {
@@ -476,7 +575,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
                             const uint32_t hi = odd ? pack_bf16x2_hi_lo(recv, hv[i + 1], lo)
                                                     : pack_bf16x2_hi_lo(hv[i], recv, lo);
                             const int tok = tb + i + odd;
-                            if (tok0 + tok < t.cnt) {
+                            if (tok < t.ntok) {  // columns past the piece belong to other pieces
                                 uint16_t* dst = out + (row0 + tok) * ld + hcol;
                                 *reinterpret_cast<uint32_t*>(dst) = hi;
                                 *reinterpret_cast<uint32_t*>(dst + 64) = lo;
@@ -497,7 +596,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const Maps* maps, con
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int tok = cc + i;
-                            if (tok0 + tok < t.cnt)
+                            if (tok < t.ntok)  // columns past the piece belong to other pieces
                                 out[(row0 + tok) * args.out_cols + col] = __uint_as_float(i < 16 ? v0[i] : v1[i - 16]);
                         }
                     }
