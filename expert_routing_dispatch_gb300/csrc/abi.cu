@@ -166,6 +166,7 @@ struct MxLayerWs {
     uint8_t *xq, *xs, *xpq, *xps;
     void* ffn_ws;
     float* y_perm;
+    unsigned* sync;  // grid-barrier words of the fused launch
     size_t dispatch_bytes, total;
 };
 
@@ -193,6 +194,7 @@ MxLayerWs carve_mx(const moe_dims* d, void* base) {
     w.xps = take(P * H / 32);
     w.ffn_ws = take(mx_ffn_scratch_bytes((long long)P, d->I));
     w.y_perm = reinterpret_cast<float*>(take(P * H * 4));
+    w.sync = reinterpret_cast<unsigned*>(take(64));
     w.total = off;
     return w;
 }
@@ -469,6 +471,14 @@ int moe_layer_mxfp8(const moe_dims* d, const uint16_t* x, const float* logits, c
     float* wt = topk_w_opt ? topk_w_opt : w.topk_w;
     cudaStream_t s = (cudaStream_t)stream;
     const int n = d->e1 - d->e0;
+    if ((long long)pairs_of(d) <= MOE_FUSED_MAX_PAIRS) {  // decode sizes: one cooperative launch
+        uint8_t* hq = static_cast<uint8_t*>(w.ffn_ws);
+        uint8_t* hs = hq + align_up(pairs_of(d) * (size_t)d->I);
+        return launched(launch_layer_mx_fused(x, logits, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q, w_down_s, out,
+                                              idx, wt, w.counts, w.offsets, w.row_pair, w.pair_row, w.xpq, w.xps, hq,
+                                              hs, w.y_perm, w.sync, d->T, d->H, d->I, d->E, d->k, d->e0, d->e1,
+                                              status_dev, s));
+    }
     int32_t* hist = static_cast<int32_t*>(w.dispatch_ws);
     if (cudaMemsetAsync(hist, 0, w.dispatch_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_route_hist(logits, d->T, d->E, d->k, idx, wt, status_dev, hist, dispatch_chunk_tokens(d->T), d->e0, n,

@@ -13,10 +13,10 @@
 //   count : per-chunk histogram of local experts (moe_layer's router produces
 //           the same histogram itself, see route.cu)
 //   place : every CTA derives the offsets and its chunk's first row per expert
-//           from all chunk histograms (a redundant prefix, no scan launch), ranks
-//           its pairs in order (match_any + popc) -> row_pair, pair_row, then
-//           copies its tokens' x rows into x_perm with 16-byte vectors, reading
-//           each token's row once however many local slots it has
+//           from all chunk histograms (a redundant prefix, no scan launch), then
+//           ranks its pairs in order (match_any + popc) -> row_pair, pair_row
+//   gather: one CTA per token copies its x row into x_perm with 16-byte vectors,
+//           reading each token's row once however many local slots it has
 // The variant without a workspace (moe_dispatch_noalloc, bottom of the file)
 // runs the original four kernels: count / scan / scatter / gather over chunks of
 // 2048 pairs, with its histograms in a fixed device array.
@@ -223,18 +223,13 @@ __global__ void __launch_bounds__(kPlaceThreads) dispatch_count_tokens_kernel(co
     for (int e = threadIdx.x; e < n; e += kPlaceThreads) hist[(size_t)blockIdx.x * n + e] = h[e];
 }
 
-constexpr int kCopyTokens = 4;  // tokens whose x rows one copy pass of the place kernel keeps in flight
-
-// x_perm may be NULL (the caller copies the rows itself, e.g. in another format).
 __global__ void __launch_bounds__(kPlaceThreads) dispatch_place_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ hist, int nchunks, int chunk_t, int T, int k,
     int e0, int n, int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_pair,
-    int32_t* __restrict__ pair_row, const uint4* __restrict__ x, int H8, uint4* __restrict__ x_perm) {
+    int32_t* __restrict__ pair_row) {
     __shared__ int tot[kMaxLocal];                // pairs of each expert, all chunks
     __shared__ int base[kMaxLocal];               // first row of each expert for this chunk
     __shared__ int cur[kPlaceWarps][kMaxLocal];   // per-warp counts, then per-warp cursors
-    __shared__ int crow[kCopyTokens][32];         // copy phase: local rows of the tokens in flight
-    __shared__ int cnr[kCopyTokens];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x;
     for (int e = tid; e < n; e += kPlaceThreads) {
@@ -336,54 +331,17 @@ __global__ void __launch_bounds__(kPlaceThreads) dispatch_place_kernel(
         }
         __syncwarp();
     }
-    if (x_perm == nullptr) return;
-    // 5. copy the x rows of this chunk's tokens to their grouped rows, kCopyTokens
-    //    tokens per pass: each token row is read once whatever its number of local
-    //    slots, and every thread keeps 2 * kCopyTokens 16-byte loads in flight
-    __syncthreads();  // pair_row of this chunk, written above, is read back below
-    for (int tb = t0; tb < t1; tb += kCopyTokens) {
-        if (warp < kCopyTokens) {
-            const int t = tb + warp;
-            const int r = (t < t1 && lane < k) ? pair_row[(size_t)t * k + lane] : -1;
-            const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
-            if (r >= 0) crow[warp][__popc(m & ((1u << lane) - 1u))] = r;
-            if (lane == 0) cnr[warp] = __popc(m);
-        }
-        __syncthreads();
-        for (int v0 = tid; v0 < H8; v0 += 2 * kPlaceThreads) {
-            uint4 val[kCopyTokens][2];
-#pragma unroll
-            for (int u = 0; u < kCopyTokens; ++u)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int v = v0 + h * kPlaceThreads;
-                    if (cnr[u] > 0 && v < H8) val[u][h] = __ldg(x + (size_t)(tb + u) * H8 + v);
-                }
-#pragma unroll
-            for (int u = 0; u < kCopyTokens; ++u)
-                for (int i = 0; i < cnr[u]; ++i) {
-                    uint4* dst = x_perm + (size_t)crow[u][i] * H8;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int v = v0 + h * kPlaceThreads;
-                        if (v < H8) dst[v] = val[u][h];
-                    }
-                }
-        }
-        __syncthreads();  // crow / cnr are rewritten by the next pass
-    }
 }
 
 }  // namespace
 
-// Chunks of at least 16 tokens, about 608 of them (four per SM of a GB300) for
-// large T, so that the row copy at the end of the place kernel spreads over every
-// SM.  Independent of the device, so workspace sizes are too; the result does not
-// depend on the chunking (the stable order is unique).
+// Chunks of at least 32 tokens, about 304 of them (two per SM of a GB300) for
+// large T.  Independent of the device, so workspace sizes are too; the result
+// does not depend on the chunking (the stable order is unique).
 int dispatch_chunk_tokens(int T) {
-    const int target = 608;
+    const int target = 304;
     const int c = (T + target - 1) / target;
-    return c < 16 ? 16 : c;
+    return c < 32 ? 32 : c;
 }
 
 size_t dispatch_scratch_bytes(long long T, int n) {
@@ -397,12 +355,14 @@ cudaError_t launch_dispatch_place(const uint16_t* x, const int32_t* topk_idx, co
                                   int32_t* pair_row, uint16_t* x_perm, cudaStream_t s) {
     const int chunk = dispatch_chunk_tokens(T);
     const int nchunks = (T + chunk - 1) / chunk;
-    // the place kernel also copies its chunk's x rows (x_perm NULL: the caller copies
-    // the rows itself, e.g. in another format)
     dispatch_place_kernel<<<nchunks, kPlaceThreads, 0, s>>>(topk_idx, hist, nchunks, chunk, T, k, e0, e1 - e0, counts,
-                                                            offsets, row_pair, pair_row,
-                                                            reinterpret_cast<const uint4*>(x), H / 8,
-                                                            reinterpret_cast<uint4*>(x_perm));
+                                                            offsets, row_pair, pair_row);
+    // the row copy wants far more CTAs than there are chunks: one CTA per token
+    // (x_perm NULL: the caller copies the rows itself, e.g. in another format).
+    // Folding the copy into the place kernel's ~200-600 CTAs was measured slower.
+    if (x_perm)
+        dispatch_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), T, H / 8, k, pair_row,
+                                                 reinterpret_cast<uint4*>(x_perm));
     return cudaGetLastError();
 }
 

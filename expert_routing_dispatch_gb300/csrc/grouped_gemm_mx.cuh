@@ -109,6 +109,20 @@ struct TileCoord {
     int e, mt, nt, cnt;
 };
 
+// Pipeline counters of one thread: ring k-blocks and accumulator tiles used so far.
+// They carry over from one GEMM phase to the next inside one launch (the fused
+// decode kernel), so that the mbarrier phases stay in step.
+struct Pipe {
+    int g;   // k-blocks through the ring
+    int it;  // tiles through the two TMEM accumulators
+};
+
+// tiles this CTA takes in the current phase (tile_start built)
+__device__ __forceinline__ int tiles_of_cta(const Ctl& c, int n) {
+    const int total = c.tile_start[n];
+    return total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+}
+
 __device__ __forceinline__ uint32_t ring_base(uint8_t* raw) { return (smem_u32(raw) + 1023u) & ~1023u; }
 __device__ __forceinline__ Ctl& ctl_of(uint8_t* raw) {
     const uint32_t b = ring_base(raw);
@@ -232,8 +246,8 @@ __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_
 //   tmA: token codes [a_rows, K], 128-row boxes; tmB0 / tmB1: weight codes with
 //   boxes of n_step rows (gate/up: W_gate / W_up) or BN rows (down: W_down twice)
 template <int MODE>
-__device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tmA, const CUtensorMap* tmB0,
-                                    const CUtensorMap* tmB1, const Args& args) {
+__device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUtensorMap* tmA,
+                                    const CUtensorMap* tmB0, const CUtensorMap* tmB1, const Args& args) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = args.n;
     volatile int* abort_flag = &c.abort_flag;
@@ -248,7 +262,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
         (void)w0;
         (void)t0;
         const uint64_t pol = l2_policy_evict_last();
-        int g = 0;
+        int g = pipe.g;
         bool ok = true;
         for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile(c, n, tile, e_hint, tc);
              tile += gridDim.x) {
@@ -290,7 +304,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
         (void)wa;
         (void)wf;
         (void)t0;
-        int g = 0, it = 0;
+        int g = pipe.g, it = pipe.it;
         bool ok = true;
         const uint32_t sf_smem = smem_u32(&c.sf[0][0][0]);
         const uint32_t tmem = c.tmem_base;  // a register copy: the asm memory clobbers would reload it
@@ -343,7 +357,11 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
         const int j = warp - 6;
         const long long b_total = (long long)n * args.w_rows;
         // stage g = k-block g % kblocks of this CTA's tile number g / kblocks; lane r = row r of each chunk
-        auto load = [&](int g, uint32_t (&w)[10]) -> bool {
+        // stage g (counted from this phase's first stage g0) = k-block g % kblocks of this
+        // CTA's tile number g / kblocks
+        const int g0 = pipe.g;
+        auto load = [&](int gabs, uint32_t (&w)[10]) -> bool {
+            const int g = gabs - g0;
             const int kb = g % args.kblocks;
             if (!next_tile(c, n, blockIdx.x + (g / args.kblocks) * (int)gridDim.x, e_hint, tc)) return false;
             const long long a_row = (long long)c.row_off[tc.e] + tc.mt * BM + lane;
@@ -351,7 +369,8 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const long long row = a_row + 32 * i;
-                w[i] = row < args.a_rows ? __ldg(args.a_s + row * args.kblocks + kb) : 0u;
+                // L2-coherent loads: the fused decode kernel writes these words earlier in the launch
+                w[i] = row < args.a_rows ? __ldcg(args.a_s + row * args.kblocks + kb) : 0u;
             }
 #pragma unroll
             for (int i = 0; i < 6; ++i) {
@@ -364,7 +383,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
                     row = b_row + 32 * i;
                     src = args.b0_s;
                 }
-                w[4 + i] = row < b_total ? __ldg(src + row * args.kblocks + kb) : 0u;
+                w[4 + i] = row < b_total ? __ldcg(src + row * args.kblocks + kb) : 0u;
             }
             return true;
         };
@@ -374,9 +393,10 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
         // two items in flight: the words of this slot's next stage and of the one after
         // it are loaded before the warp waits for the slot to free up
         uint32_t w[10], wn[10];
-        bool have = load(j, w);
-        bool have_n = have && load(j + STAGES, wn);
-        for (int g = j; have && !*abort_flag; g += STAGES) {
+        const int gj = g0 + (((j - g0) % STAGES) + STAGES) % STAGES;  // first stage of slot j in this phase
+        bool have = load(gj, w);
+        bool have_n = have && load(gj + STAGES, wn);
+        for (int g = gj; have && !*abort_flag; g += STAGES) {
             const int r = g / STAGES;
             // the copies of this slot's previous round have completed with its MMAs
             if (!MX_PROF_WAIT(wsf, mbar_wait_bounded(smem_u32(&c.empty[j]), (r & 1) ^ 1, abort_flag, args.status,
@@ -403,7 +423,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
         long long wt = 0, t0 = clock64();
         (void)wt;
         (void)t0;
-        int it = 0;
+        int it = pipe.it;
         for (int tile = blockIdx.x; !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++it) {
             const int acc = it & 1, use = it >> 1;
             if (!MX_PROF_WAIT(wt, mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status,
@@ -485,6 +505,13 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, const CUtensorMap* tm
             MX_PROF_ADD(7, clock64() - t0);
         }
     }
+}
+
+// Every thread: its counters after a phase that ran to completion.
+__device__ __forceinline__ void pipe_advance(const Ctl& c, Pipe& p, int n, int kblocks) {
+    const int nt = tiles_of_cta(c, n);
+    p.g += nt * kblocks;
+    p.it += nt;
 }
 
 // After a __syncthreads: drain the MMAs (bounded), free TMEM.  Every load the

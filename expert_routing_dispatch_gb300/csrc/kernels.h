@@ -80,6 +80,15 @@ cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int
                                  const uint8_t* wds, float* y_perm, long long rows, int H, int I, int n,
                                  void* scratch, int32_t* status, cudaStream_t s, int stall_gate_up = 0);
 
+// mxfp8.cu: the MXFP8 layer in one persistent cooperative launch (decode sizes);
+// sync[0..1] are cleared on the stream by the launcher
+cudaError_t launch_layer_mx_fused(const uint16_t* x, const float* logits, const uint8_t* wgq, const uint8_t* wgs,
+                                  const uint8_t* wuq, const uint8_t* wus, const uint8_t* wdq, const uint8_t* wds,
+                                  float* out, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                  int32_t* row_pair, int32_t* pair_row, uint8_t* xpq, uint8_t* xps, uint8_t* hq,
+                                  uint8_t* hs, float* y_perm, unsigned* sync, int T, int H, int I, int E, int k,
+                                  int e0, int e1, int32_t* status, cudaStream_t s);
+
 // device query shared by the launchers
 int sm_count();
 

@@ -7,8 +7,10 @@
 //   gate/up  : block-scaled tcgen05 GEMM, SiLU*up, h quantised to MXFP8 in the epilogue
 //   down     : block-scaled tcgen05 GEMM -> y_perm (fp32)
 // The GEMM core is in grouped_gemm_mx.cuh.
+#include "combine.cuh"
 #include "grouped_gemm_mx.cuh"
 #include "kernels.h"
+#include "route.cuh"
 
 namespace moe {
 
@@ -87,9 +89,289 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    mx::run<MODE>(c, ring, &tmA, &tmB0, &tmB1, args);
+    mx::Pipe pipe{0, 0};
+    mx::run<MODE>(c, ring, pipe, &tmA, &tmB0, &tmB1, args);
     __syncthreads();
     mx::teardown(c, args.status);
+}
+
+// ------------------------------------------------------------------ fused decode
+// "Hosting Qwen on Blackwell", section "Expert Parallel": for decode the whole
+// expert-parallel kernel is one fused kernel.  The MXFP8 layer in one cooperative
+// launch of one CTA per SM, phases separated by bounded grid-wide barriers:
+//   P0 route; P1 dispatch (every CTA counts all pairs, scatters its own token slice,
+//   quantises each of its tokens' x rows to MXFP8 once and writes the codes and
+//   scales to every local row); P2 MX gate/up; P3 MX down; P4 combine.  The MX GEMM
+//   core (grouped_gemm_mx.cuh) keeps its ring and accumulator counters across P2
+//   and P3.  sync[0] (arrivals) and sync[1] (abort) are zero at launch.
+constexpr long long MX_GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
+
+struct MxFusedArgs {
+    const float* logits;
+    const uint4* x;  // bf16 [T, H] as 16-byte vectors
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* row_pair;
+    int32_t* pair_row;
+    uint8_t* xpq;  // [T*k, H] E4M3 codes of the grouped rows
+    uint8_t* xps;  // [T*k, H/32] their scales
+    uint8_t* hq;   // [T*k, I]
+    uint8_t* hs;   // [T*k, I/32]
+    const uint8_t* wgs;
+    const uint8_t* wus;
+    const uint8_t* wds;
+    float* y_perm;
+    float* out;
+    unsigned* sync;
+    int32_t* status;
+    int T, H, I, E, k, e0, e1;
+};
+
+struct MxFusedSmem {
+    int hist_before[mx::MAX_LOCAL];  // local pairs of each expert before this CTA's slice
+    int cursor[mx::MAX_LOCAL];       // next grouped row of each expert for this CTA
+    int rows[32];
+    CombineSmem comb;
+    int ok;
+};
+constexpr size_t MX_FUSED_SMEM_BYTES = mx::SMEM_BYTES + sizeof(MxFusedSmem);
+static_assert(MX_FUSED_SMEM_BYTES <= 232448, "fused MXFP8 kernel exceeds the 227 KB shared-memory limit");
+
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier (all CTAs co-resident): false, uniformly over the CTA, on
+// timeout or when another CTA aborted.
+__device__ bool mx_grid_sync(const MxFusedArgs& a, unsigned target, MxFusedSmem& fs) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        __threadfence();
+        atomicAdd(&a.sync[0], 1u);
+        const long long t0 = clock64();
+        for (;;) {
+            if (ld_acquire_gpu_u32(&a.sync[0]) >= target) break;
+            if (ld_acquire_gpu_u32(&a.sync[1]) != 0u) {
+                ok = 0;
+                break;
+            }
+            if (clock64() - t0 > MX_GRID_WAIT_LIMIT) {
+                atomicExch(&a.sync[1], 1u);
+                set_status(a.status, MOE_ERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
+            __nanosleep(128);
+        }
+        __threadfence();
+        fs.ok = ok;
+    }
+    __syncthreads();
+    return fs.ok != 0;
+}
+
+__global__ void __launch_bounds__(mx::NUM_THREADS, 1)
+    moe_layer_mx_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
+                              const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
+                              const __grid_constant__ CUtensorMap tmD, const MxFusedArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t ring = mx::ring_base(smem_raw);
+    mx::Ctl& c = mx::ctl_of(smem_raw);
+    MxFusedSmem& fs = *reinterpret_cast<MxFusedSmem*>(reinterpret_cast<uint8_t*>(&c) + sizeof(mx::Ctl));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = a.e1 - a.e0, T = a.T, k = a.k;
+    const unsigned G = gridDim.x;
+
+    mx::init(c, 0);
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmG);
+        tma_prefetch_desc(&tmU);
+        tma_prefetch_desc(&tmH);
+        tma_prefetch_desc(&tmD);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    mx::Pipe pipe{0, 0};
+
+    // ---------------- P0: route
+    {
+        const int warps = mx::NUM_THREADS / 32;
+        for (int t = blockIdx.x * warps + warp; t < T; t += G * warps)
+            route_token_any(a.logits, t, a.E, k, a.topk_idx, a.topk_w, a.status);
+    }
+    bool ok = mx_grid_sync(a, 1u * G, fs);
+
+    // ---------------- P1: dispatch, x quantised to MXFP8 once per token
+    if (ok) {
+        const long long P = (long long)T * k;
+        const int tpc = (T + (int)G - 1) / (int)G;
+        const int t0 = min(T, (int)blockIdx.x * tpc), t1 = min(T, t0 + tpc);
+        const long long p0 = (long long)t0 * k, p1 = (long long)t1 * k;
+        int* hist_all = c.tile_start;  // scratch until the tile table is built
+        for (int e = threadIdx.x; e < n; e += mx::NUM_THREADS) {
+            hist_all[e] = 0;
+            fs.hist_before[e] = 0;
+        }
+        __syncthreads();
+        for (long long q = threadIdx.x; q < P; q += mx::NUM_THREADS) {
+            const int e = __ldcg(a.topk_idx + q) - a.e0;
+            if (e >= 0 && e < n) {
+                atomicAdd(&hist_all[e], 1);
+                if (q < p0) atomicAdd(&fs.hist_before[e], 1);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {  // exclusive scan -> row_off
+            int carry = 0;
+            for (int b0 = 0; b0 < n; b0 += 32) {
+                const int e = b0 + lane;
+                const int v0 = (e < n) ? hist_all[e] : 0;
+                int v = v0;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += y;
+                }
+                if (e < n) c.row_off[e] = carry + v - v0;
+                carry += __shfl_sync(0xffffffffu, v, 31);
+            }
+            if (lane == 0) c.row_off[n] = carry;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < n; e += mx::NUM_THREADS) {
+            fs.cursor[e] = c.row_off[e] + fs.hist_before[e];
+            if (blockIdx.x == 0) {
+                a.counts[e] = hist_all[e];
+                a.offsets[e] = c.row_off[e];
+            }
+        }
+        if (blockIdx.x == 0 && threadIdx.x == 0) a.offsets[n] = c.row_off[n];
+        __syncthreads();
+        if (warp == 0) {  // this CTA's pairs, in pair order
+            const unsigned lt = (1u << lane) - 1u;
+            for (long long b = p0; b < p1; b += 32) {
+                const long long q = b + lane;
+                const bool valid = q < p1;
+                const int e = valid ? __ldcg(a.topk_idx + q) - a.e0 : -1;
+                const bool local = valid && e >= 0 && e < n;
+                const unsigned peers = __match_any_sync(0xffffffffu, local ? e : -1);
+                const int base = local ? fs.cursor[e] : 0;
+                __syncwarp();
+                if (local) {
+                    const int row = base + __popc(peers & lt);
+                    if ((peers & lt) == 0) fs.cursor[e] = base + __popc(peers);
+                    a.row_pair[row] = (int32_t)q;
+                    a.pair_row[q] = row;
+                } else if (valid) {
+                    a.pair_row[q] = -1;
+                }
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        const int H8 = a.H / 8, nblk = a.H / 32;
+        for (int t = t0; t < t1; ++t) {  // quantise each token row once, copy to its local rows
+            if (threadIdx.x < 32) {
+                const int r = (lane < k) ? a.pair_row[(size_t)t * k + lane] : -1;
+                const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
+                if (r >= 0) fs.rows[__popc(m & ((1u << lane) - 1u))] = r;
+                if (lane == 0) fs.comb.nrows = __popc(m);
+            }
+            __syncthreads();
+            const int nr = fs.comb.nrows;
+            for (int b = threadIdx.x; nr > 0 && b < nblk; b += mx::NUM_THREADS) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 u = __ldg(a.x + (size_t)t * H8 + b * 4 + i);
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        v[8 * i + 2 * j] = bf16_lo(w4[j]);
+                        v[8 * i + 2 * j + 1] = bf16_hi(w4[j]);
+                    }
+                }
+                uint32_t w[8];
+                const uint8_t code = (uint8_t)mx::mx_quantize32(v, w);
+                for (int i = 0; i < nr; ++i) {
+                    const size_t row = (size_t)fs.rows[i];
+                    uint4* dst = reinterpret_cast<uint4*>(a.xpq + row * a.H + 32 * b);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    a.xps[row * nblk + b] = code;
+                }
+            }
+            __syncthreads();
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // xpq is read by TMA next
+        ok = mx_grid_sync(a, 2u * G, fs);
+    }
+
+    // ---------------- P2: MX gate/up GEMM + SiLU*up, h quantised to MXFP8
+    if (ok) {
+        const int nt = (a.I + mx::BN / 2 - 1) / (mx::BN / 2);
+        const mx::Args ga{a.hq,
+                          a.hs,
+                          reinterpret_cast<const uint32_t*>(a.xps),
+                          reinterpret_cast<const uint32_t*>(a.wgs),
+                          reinterpret_cast<const uint32_t*>(a.wus),
+                          (long long)T * k,
+                          a.status,
+                          n,
+                          a.H / mx::BKB,
+                          nt,
+                          a.I,
+                          a.I,
+                          mx::BN / 2,
+                          0};
+        mx::build_tile_table(c, n, nt);
+        __syncthreads();
+        mx::run<mx::MODE_GATEUP>(c, ring, pipe, &tmX, &tmG, &tmU, ga);
+        mx::pipe_advance(c, pipe, n, ga.kblocks);
+        ok = mx_grid_sync(a, 3u * G, fs) && !c.abort_flag;
+    }
+
+    // ---------------- P3: MX down GEMM
+    if (ok) {
+        const int nt = (a.H + mx::BN - 1) / mx::BN;
+        const mx::Args da{a.y_perm,
+                          nullptr,
+                          reinterpret_cast<const uint32_t*>(a.hs),
+                          reinterpret_cast<const uint32_t*>(a.wds),
+                          reinterpret_cast<const uint32_t*>(a.wds),
+                          (long long)T * k,
+                          a.status,
+                          n,
+                          a.I / mx::BKB,
+                          nt,
+                          a.H,
+                          a.H,
+                          mx::BN,
+                          0};
+        mx::build_tile_table(c, n, nt);
+        __syncthreads();
+        mx::run<mx::MODE_DOWN>(c, ring, pipe, &tmH, &tmD, &tmD, da);
+        mx::pipe_advance(c, pipe, n, da.kblocks);
+        ok = mx_grid_sync(a, 4u * G, fs) && !c.abort_flag;
+    }
+
+    // ---------------- P4: combine
+    if (ok) {
+        const int H4 = a.H / 4;
+        for (int t = blockIdx.x; t < T; t += G)
+            combine_token(reinterpret_cast<const float4*>(a.y_perm), a.pair_row, a.topk_w, t, H4, k,
+                          reinterpret_cast<float4*>(a.out), fs.comb, true);
+    }
+
+    __syncthreads();
+    mx::teardown(c, a.status);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -135,6 +417,39 @@ cudaError_t launch_mx_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CU
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 }  // namespace
+
+cudaError_t launch_layer_mx_fused(const uint16_t* x, const float* logits, const uint8_t* wgq, const uint8_t* wgs,
+                                  const uint8_t* wuq, const uint8_t* wus, const uint8_t* wdq, const uint8_t* wds,
+                                  float* out, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                  int32_t* row_pair, int32_t* pair_row, uint8_t* xpq, uint8_t* xps, uint8_t* hq,
+                                  uint8_t* hs, float* y_perm, unsigned* sync, int T, int H, int I, int E, int k,
+                                  int e0, int e1, int32_t* status, cudaStream_t s) {
+    const cudaError_t attr =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(&moe_layer_mx_fused_kernel), (int)MX_FUSED_SMEM_BYTES);
+    if (attr != cudaSuccess) return attr;
+    const int n = e1 - e0;
+    const long long rows = (long long)T * k;
+    CUtensorMap mX, mG, mU, mH, mD;
+    if (!make_tmap_u8(&mX, xpq, rows, H, mx::BM) || !make_tmap_u8(&mG, wgq, (long long)n * I, H, mx::BN / 2) ||
+        !make_tmap_u8(&mU, wuq, (long long)n * I, H, mx::BN / 2) || !make_tmap_u8(&mH, hq, rows, I, mx::BM) ||
+        !make_tmap_u8(&mD, wdq, (long long)n * H, I, mx::BN))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    MxFusedArgs a{logits, reinterpret_cast<const uint4*>(x), topk_idx, topk_w, counts, offsets, row_pair, pair_row,
+                  xpq, xps, hq, hs, wgs, wus, wds, y_perm, out, sync, status, T, H, I, E, k, e0, e1};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sm_count());
+    cfg.blockDim = dim3(mx::NUM_THREADS);
+    cfg.dynamicSmemBytes = MX_FUSED_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_layer_mx_fused_kernel, mX, mG, mU, mH, mD, a);
+}
 
 cudaError_t launch_mx_quantize(const uint16_t* src, long long rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st) {
     const long long blocks = rows * (K / 32);

@@ -287,10 +287,13 @@ int moe_testing_expert_ffn_mxfp8_stalled(const moe_dims* d, const uint8_t* x_per
 
 /*
  * The whole local layer with MXFP8 expert weights: route, dispatch (x quantised to
- * MXFP8 once per token, rows gathered in that format), the MXFP8 expert FFN and the
- * weighted fp32 combine into out fp32 [T, H].  Always the split kernels (no fused
- * decode launch).  Routing, counts, offsets and the permutation are those of
- * moe_layer.  ws >= moe_layer_mxfp8_workspace_size(d) bytes, 256-byte aligned.
+ * MXFP8 once per token, rows copied in that format), the MXFP8 expert FFN and the
+ * weighted fp32 combine into out fp32 [T, H].  As for moe_layer ("Expert Parallel"
+ * section): T*k <= MOE_FUSED_MAX_PAIRS runs one persistent cooperative launch with
+ * bounded grid-wide barriers between the phases (plus an 8-byte memset of its
+ * barrier words), larger problems the split kernels; both give bit-identical
+ * results.  Routing, counts, offsets and the permutation are those of moe_layer.
+ * ws >= moe_layer_mxfp8_workspace_size(d) bytes, 256-byte aligned.
  */
 size_t moe_layer_mxfp8_workspace_size(const moe_dims* d);
 int moe_layer_mxfp8(const moe_dims* d, const uint16_t* x, const float* logits, const uint8_t* w_gate_q,

@@ -166,7 +166,7 @@ def test_mx_expert_ffn(moe, name):
     assert (diff <= bound + FP32_SLACK * rms_all).all()
 
 
-@pytest.mark.parametrize("name", ["tiny", "prefill_ep_rank", "skewed"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill_ep_rank", "skewed"])
 def test_mx_layer(moe, name):
     import torch
 
@@ -276,3 +276,72 @@ def test_mx_layer_small_shapes(moe, dims):
           f"{(diff / (bound + FP32_SLACK * rms)).max():.3f}")
     assert (diff <= bound * (1 + 1e-6) + FP32_SLACK * rms).all()
 
+
+
+def _mx_layer(moe, dims, inp, w):
+    import torch
+
+    T, H, I, E, k, e0, e1 = (dims.T, dims.H, dims.I, dims.E, dims.k, dims.e0, dims.e1)
+    dw = {key: (dev(q), dev(s)) for key, (q, s) in w.items()}
+    out = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    idx = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = moe.alloc_workspace(moe.moe_layer_mxfp8_workspace_size(dims))
+    moe.moe_layer_mxfp8(dims, dev(inp["x"]), dev(inp["logits"]), dw["w_gate"], dw["w_up"], dw["w_down"], out, ws,
+                        topk_idx=idx, topk_w=wt, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return host(out), host(idx), host(wt)
+
+
+def _mx_split_entries(moe, dims, inp, w):
+    """moe_route, moe_dispatch (bf16 rows), moe_quantize_mxfp8 of the grouped rows,
+    moe_expert_ffn_mxfp8 and moe_combine, composed by hand."""
+    import torch
+
+    T, H, I, E, k, e0, e1 = (dims.T, dims.H, dims.I, dims.E, dims.k, dims.e0, dims.e1)
+    n, P = e1 - e0, T * k
+    z = lambda shape, dt: torch.zeros(shape, dtype=dt, device="cuda")
+    dw = {key: (dev(q), dev(s)) for key, (q, s) in w.items()}
+    idx, wt, st = z((T, k), torch.int32), z((T, k), torch.float32), z(1, torch.int32)
+    counts, offsets, row_pair, pair_row = z(n, torch.int32), z(n + 1, torch.int32), z(P, torch.int32), z(P, torch.int32)
+    x_perm, y, out = z((P, H), torch.int16), z((P, H), torch.float32), z((T, H), torch.float32)
+    xq, xs = z((P, H), torch.uint8), z((P, H // 32), torch.uint8)
+    moe.moe_route(dims, dev(inp["logits"]), idx, wt, st)
+    moe.moe_dispatch(dims, dev(inp["x"]), idx, counts, offsets, row_pair, pair_row, x_perm,
+                     moe.alloc_workspace(moe.moe_dispatch_workspace_size(dims)))
+    moe.moe_quantize_mxfp8(x_perm, P, H, xq, xs)
+    moe.moe_expert_ffn_mxfp8(dims, xq, xs, offsets, dw["w_gate"], dw["w_up"], dw["w_down"], y,
+                             moe.alloc_workspace(moe.moe_expert_ffn_mxfp8_workspace_size(dims)), status=st)
+    moe.moe_combine(dims, y, pair_row, wt, out)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return host(out), host(idx), host(wt)
+
+
+@pytest.mark.parametrize("name", ["decode", "tiny"])
+def test_mx_fused_equals_split_bit_for_bit(moe, name):
+    # T*k <= MOE_FUSED_MAX_PAIRS: moe_layer_mxfp8 is one cooperative launch (x quantised per
+    # token inside it); the split entries must give the same bytes
+    cfg, inp = inputs(name)
+    dims = moe.Dims.of(cfg)
+    assert dims.T * dims.k <= moe.FUSED_MAX_PAIRS
+    w = mx_weights(name)
+    a, ia, wa = _mx_layer(moe, dims, inp, w)
+    b, ib, wb = _mx_split_entries(moe, dims, inp, w)
+    assert np.array_equal(ia, ib) and np.array_equal(wa.view(np.uint32), wb.view(np.uint32))
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_mx_layer_split_path_equals_split_entries(moe):
+    # above the threshold moe_layer_mxfp8 runs its split kernels (x quantised before the row
+    # copy); composing the public entries must give the same bytes
+    cfg, inp = inputs("prefill_ep_rank")
+    dims = moe.Dims.of(cfg)
+    assert dims.T * dims.k > moe.FUSED_MAX_PAIRS
+    w = mx_weights("prefill_ep_rank")
+    a, ia, wa = _mx_layer(moe, dims, inp, w)
+    b, ib, wb = _mx_split_entries(moe, dims, inp, w)
+    assert np.array_equal(ia, ib)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
