@@ -41,6 +41,7 @@ L2_FLUSH_BYTES = 256 << 20
 _CS = "expert_routing_dispatch_gb300/csrc/"
 KERNEL_SOURCES = {
     "grouped_gemm_gate_up": [_CS + "grouped_ffn.cu", _CS + "grouped_gemm_pair.cuh", _CS + "common.cuh"],
+    "grouped_gemm_down": [_CS + "grouped_ffn.cu", _CS + "grouped_gemm_pair.cuh", _CS + "common.cuh"],
     "grouped_ffn_mx": [_CS + "mxfp8.cu", _CS + "grouped_gemm_mx.cuh", _CS + "common.cuh"],
     "moe_layer_fused": [_CS + "decode_fused.cu", _CS + "grouped_gemm.cuh", _CS + "common.cuh", _CS + "route.cuh",
                         _CS + "combine.cuh"],
@@ -143,6 +144,10 @@ def recorded_traffic(kernel, config):
         return float(kv["dram_bytes_per_launch_full_size"])
     except (KeyError, ValueError):
         return None
+
+
+def sum_or_none(*vals):
+    return None if any(v is None for v in vals) else float(sum(vals))
 
 
 class ClockSampler:
@@ -568,7 +573,8 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     flop_gate_up = 4.0 * H * I * R
     flop_layer = 6.0 * H * I * R
-    weight_bytes = 3.0 * H * I * 2 * active
+    # weight bytes streamed per step: bf16, or E4M3 codes plus one UE8M0 scale per 32
+    weight_bytes = 3.0 * H * I * (1.0 + 1.0 / 32 if mx else 2.0) * active
     if fused:
         # HBM roofline of the fused launch: active experts' weights streamed once,
         # plus x, logits and the fp32 output (intermediates stay in L2)
@@ -601,8 +607,11 @@ def run_ours(args):
                     "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst (cuBLAS)",
                     "frac_of_nominal_dense": achieved / NOMINAL_BF16_DENSE_TFLOPS,
                     "nominal_dense_peak": NOMINAL_BF16_DENSE_TFLOPS,
-                    "traffic": recorded_traffic("grouped_gemm_gate_up", args.config),
-                    "traffic_note": "DRAM bytes of the gate/up launch alone (ncu)",
+                    "traffic": sum_or_none(recorded_traffic("grouped_gemm_gate_up", args.config),
+                                           recorded_traffic("grouped_gemm_down", args.config)),
+                    "traffic_note": "DRAM bytes of the gate/up and down launches (ncu), per step",
+                    "algorithmic_bytes": (2 * H * I * 2 * active + R * H * 2 + R * 2 * I * 2) +
+                                         (H * I * 2 * active + R * 2 * I * 2 + R * H * 4),
                     "algorithmic_flop_per_launch": flop_layer,
                     "gate_up": {"achieved": gu, "frac": gu / peaks["bf16_tflops"],
                                 "frac_of_nominal_dense": gu / NOMINAL_BF16_DENSE_TFLOPS, "flop": flop_gate_up},

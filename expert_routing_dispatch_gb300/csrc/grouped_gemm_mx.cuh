@@ -103,6 +103,7 @@ struct Args {
     int w_rows;              // weight rows per expert (I or H)
     int n_step;              // output columns per n-tile: 96 (gate/up) or 192 (down)
     int stall;               // testing hook: extra arrivals ring stage 0 waits for (0 in normal use)
+    int a_small;             // box rows of the optional small token map (0 = none)
 };
 
 struct TileCoord {
@@ -243,11 +244,15 @@ __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_
 }
 
 // One GEMM over all tiles; every thread of the CTA calls it and plays its role.
-//   tmA: token codes [a_rows, K], 128-row boxes; tmB0 / tmB1: weight codes with
+//   tmA: token codes [a_rows, K], 128-row boxes (tmA_small, optional: the same codes
+//   with args.a_small-row boxes, loaded for m-tiles with that few rows; the MMA still
+//   reads 128 rows and the stale ones only feed output rows that are not stored);
+//   tmB0 / tmB1: weight codes with
 //   boxes of n_step rows (gate/up: W_gate / W_up) or BN rows (down: W_down twice)
 template <int MODE>
 __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUtensorMap* tmA,
-                                    const CUtensorMap* tmB0, const CUtensorMap* tmB1, const Args& args) {
+                                    const CUtensorMap* tmB0, const CUtensorMap* tmB1, const Args& args,
+                                    const CUtensorMap* tmA_small = nullptr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = args.n;
     volatile int* abort_flag = &c.abort_flag;
@@ -267,6 +272,9 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUt
         for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile(c, n, tile, e_hint, tc);
              tile += gridDim.x) {
             const int a_row = c.row_off[tc.e] + tc.mt * BM;
+            const bool small = tmA_small != nullptr && tc.cnt - tc.mt * BM <= args.a_small;
+            const CUtensorMap* tma = small ? tmA_small : tmA;
+            const uint32_t stage_tx = (uint32_t)((small ? args.a_small : BM) * BKB + B_BYTES);
             const int b_row = tc.e * args.w_rows + tc.nt * args.n_step;
             for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
                 const int s = g % STAGES, r = g / STAGES;
@@ -278,13 +286,13 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUt
                 if (elect_one()) {
                     // gate/up: weight boxes before the token box; down: token box first
                     const uint32_t fb = smem_u32(&c.full[s]);
-                    mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
+                    mbar_arrive_expect_tx(fb, stage_tx);
                     if (MODE == MODE_GATEUP) {  // [96 gate rows | 96 up rows]
                         tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
                         tma_load_2d(b_addr(s) + (uint32_t)(BN / 2) * BKB, tmB1, kb * BKB, b_row, fb, pol);
-                        tma_load_2d(a_addr(s), tmA, kb * BKB, a_row, fb, pol);
+                        tma_load_2d(a_addr(s), tma, kb * BKB, a_row, fb, pol);
                     } else {
-                        tma_load_2d(a_addr(s), tmA, kb * BKB, a_row, fb, pol);
+                        tma_load_2d(a_addr(s), tma, kb * BKB, a_row, fb, pol);
                         tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
                     }
                 }

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
 //   core (grouped_gemm_mx.cuh) keeps its ring and accumulator counters across P2
 //   and P3.  sync[0] (arrivals) and sync[1] (abort) are zero at launch.
 constexpr long long MX_GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
+constexpr int MX_SMALL_ROWS = 32;                     // rows of the small token-tile boxes
 
 struct MxFusedArgs {
     const float* logits;
@@ -178,7 +179,10 @@ __device__ bool mx_grid_sync(const MxFusedArgs& a, unsigned target, MxFusedSmem&
 __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
     moe_layer_mx_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
                               const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
-                              const __grid_constant__ CUtensorMap tmD, const MxFusedArgs a) {
+                              const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmXs,
+                              const __grid_constant__ CUtensorMap tmHs, const MxFusedArgs a) {
+    // tmXs / tmHs: the x and h codes with MX_SMALL_ROWS-row boxes, for m-tiles with that
+    // few rows (decode has ~16 rows per expert: a quarter of the token-tile bytes)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t ring = mx::ring_base(smem_raw);
     mx::Ctl& c = mx::ctl_of(smem_raw);
@@ -194,6 +198,8 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
         tma_prefetch_desc(&tmU);
         tma_prefetch_desc(&tmH);
         tma_prefetch_desc(&tmD);
+        tma_prefetch_desc(&tmXs);
+        tma_prefetch_desc(&tmHs);
     }
     tc_fence_before();
     __syncthreads();
@@ -330,10 +336,11 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
                           a.I,
                           a.I,
                           mx::BN / 2,
-                          0};
+                          0,
+                          MX_SMALL_ROWS};
         mx::build_tile_table(c, n, nt);
         __syncthreads();
-        mx::run<mx::MODE_GATEUP>(c, ring, pipe, &tmX, &tmG, &tmU, ga);
+        mx::run<mx::MODE_GATEUP>(c, ring, pipe, &tmX, &tmG, &tmU, ga, &tmXs);
         mx::pipe_advance(c, pipe, n, ga.kblocks);
         ok = mx_grid_sync(a, 3u * G, fs) && !c.abort_flag;
     }
@@ -354,10 +361,11 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
                           a.H,
                           a.H,
                           mx::BN,
-                          0};
+                          0,
+                          MX_SMALL_ROWS};
         mx::build_tile_table(c, n, nt);
         __syncthreads();
-        mx::run<mx::MODE_DOWN>(c, ring, pipe, &tmH, &tmD, &tmD, da);
+        mx::run<mx::MODE_DOWN>(c, ring, pipe, &tmH, &tmD, &tmD, da, &tmHs);
         mx::pipe_advance(c, pipe, n, da.kblocks);
         ok = mx_grid_sync(a, 4u * G, fs) && !c.abort_flag;
     }
@@ -429,10 +437,11 @@ cudaError_t launch_layer_mx_fused(const uint16_t* x, const float* logits, const 
     if (attr != cudaSuccess) return attr;
     const int n = e1 - e0;
     const long long rows = (long long)T * k;
-    CUtensorMap mX, mG, mU, mH, mD;
+    CUtensorMap mX, mG, mU, mH, mD, mXs, mHs;
     if (!make_tmap_u8(&mX, xpq, rows, H, mx::BM) || !make_tmap_u8(&mG, wgq, (long long)n * I, H, mx::BN / 2) ||
         !make_tmap_u8(&mU, wuq, (long long)n * I, H, mx::BN / 2) || !make_tmap_u8(&mH, hq, rows, I, mx::BM) ||
-        !make_tmap_u8(&mD, wdq, (long long)n * H, I, mx::BN))
+        !make_tmap_u8(&mD, wdq, (long long)n * H, I, mx::BN) || !make_tmap_u8(&mXs, xpq, rows, H, MX_SMALL_ROWS) ||
+        !make_tmap_u8(&mHs, hq, rows, I, MX_SMALL_ROWS))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
@@ -448,7 +457,7 @@ cudaError_t launch_layer_mx_fused(const uint16_t* x, const float* logits, const 
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_layer_mx_fused_kernel, mX, mG, mU, mH, mD, a);
+    return cudaLaunchKernelEx(&cfg, moe_layer_mx_fused_kernel, mX, mG, mU, mH, mD, mXs, mHs, a);
 }
 
 cudaError_t launch_mx_quantize(const uint16_t* src, long long rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st) {
@@ -496,7 +505,8 @@ cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int
                       I,
                       I,
                       mx::BN / 2,
-                      stall_gate_up};
+                      stall_gate_up,
+                      0};
     cudaError_t e = launch_mx_gemm<mx::MODE_GATEUP>(mX, mG, mU, offsets, ga, s);
     if (e != cudaSuccess) return e;
     const mx::Args da{y_perm,
@@ -512,6 +522,7 @@ cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int
                       H,
                       H,
                       mx::BN,
+                      0,
                       0};
     return launch_mx_gemm<mx::MODE_DOWN>(mH, mD, mD, offsets, da, s);
 }
