@@ -18,16 +18,18 @@
 // n / 32 of the B slot, repeated in every 32-lane quadrant (each quadrant of
 // accumulator rows reads the B scales from its own lanes).
 //
-// CTA = 10 warps: warp 0 issues the TMA loads of the E4M3 tiles into a 4-stage
-// ring; warp 1 owns TMEM (two 192-column accumulators and four 12-column scale
-// slots) and one of its threads issues, per k-block, three tcgen05.cp of the
-// stage's scale words (shared memory -> TMEM, each 32 rows x 16 bytes copied to
-// all four lane quadrants) and the four MMAs, in order in the tensor pipe;
-// warps 2..5 run the epilogue; warps 6..9 gather the scale words from global
-// memory into the shared-memory chunks of ring slot warp - 6 (each warp owns one
-// slot and keeps the words of its next two stages in registers, loading the
-// second right after publishing one, so the loads have eight stages of MMAs to
-// land before they are needed).
+// CTA = 10 warps: warp 0 issues the TMA loads of the E4M3 tiles into the ring
+// (4 stages of 128 token rows + 192 weight rows for the split path, 6 stages of
+// 32 token rows + 192 weight rows for the fused decode, see Geo below); warp 1
+// owns TMEM (two 192-column accumulators and one 12-column scale slot per stage)
+// and one of its threads issues, per k-block, three tcgen05.cp of the stage's
+// scale words (shared memory -> TMEM, each 32 rows x 16 bytes copied to all four
+// lane quadrants) and the four MMAs, in order in the tensor pipe; warps 2..5 run
+// the epilogue; warps 6..9 gather the scale words from global memory into the
+// shared-memory chunks of the ring: warp 6 + j fills the stages g with g % 4 == j
+// and keeps the words of its next two stages in registers, loading the second
+// right after publishing one, so the loads have eight stages of MMAs to land
+// before they are needed.
 // Every wait is bounded.
 #pragma once
 
@@ -36,18 +38,34 @@
 namespace moe {
 namespace mx {
 
-constexpr int BM = 128, BN = 192, BKB = 128;  // k-block: 128 E4M3 = 128 bytes per row
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BKB;              // 16 KB
+constexpr int BM = 128, BN = 192, BKB = 128;  // MMA shape M x N; k-block: 128 E4M3 = 128 bytes per row
 constexpr int B_BYTES = BN * BKB;              // 24 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 40 KB
 constexpr int NUM_THREADS = 320;
+constexpr int SCALE_WARPS = 4;
 constexpr int ACC_COLS = BN;
 constexpr int SF_COL0 = 2 * ACC_COLS;  // first scale slot column (384)
 constexpr int SF_SLOT = 12;            // columns per slot: 4 for A, 6 (of 8) for B
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_LOCAL = 1024;
 constexpr long long WAIT_LIMIT = 1ll << 31;
+
+// Ring geometry: AR token rows per m-tile (the rows of a stage's A slot) and S
+// stages.  The MMA always has M = 128; with AR = 32 its A rows 32..127 read the
+// bytes after the A slot (inside the ring) and only feed accumulator rows that
+// are never stored, so a stage carries 4 KB of tokens instead of 16 KB and more
+// stages of weights fit in shared memory.
+template <int AR_, int S_>
+struct Geo {
+    static constexpr int AR = AR_;
+    static constexpr int STAGES = S_;
+    static constexpr int A_BYTES = AR * BKB;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static_assert(AR == 32 || AR == 128, "m-tiles of 32 or 128 token rows");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the 128-byte swizzle");
+    static_assert(SF_COL0 + S_ * SF_SLOT <= TMEM_COLS, "scale slots exceed the TMEM allocation");
+};
+using GeoPrefill = Geo<128, 4>;  // split path: 128-token m-tiles, 4 stages of 40 KB
+using GeoDecode = Geo<32, 6>;    // fused decode: 32-token m-tiles, 6 stages of 28 KB (144 KB of weights in flight)
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
@@ -71,12 +89,13 @@ __device__ unsigned long long g_mx_prof[2][12];
 #define MX_PROF_ADD(i, v) ((void)0)
 #endif
 
+template <int S>
 struct Ctl {
     alignas(128) uint4 stage[4][32 * 8];  // down epilogue: 32-row x 128-byte fp32 staging per warp
     // scale words per ring stage: [A | B columns 0-3 | B columns 4-5, 2 spare], each 32 rows x 16 bytes
-    alignas(128) uint4 sf[STAGES][3][32];
-    uint64_t full[STAGES];  // the stage's TMA bytes (producer's expect-tx arrival) and its scale chunk (scale warp)
-    uint64_t empty[STAGES];
+    alignas(128) uint4 sf[S][3][32];
+    uint64_t full[S];  // the stage's TMA bytes (producer's expect-tx arrival) and its scale chunk (scale warp)
+    uint64_t empty[S];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -85,8 +104,11 @@ struct Ctl {
     int tile_start[MAX_LOCAL + 1];
     int row_off[MAX_LOCAL + 1];
 };
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
-static_assert(SMEM_BYTES <= 232448, "MX GEMM exceeds the 227 KB shared-memory limit");
+template <class G>
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)G::STAGES * G::STAGE_BYTES + sizeof(Ctl<G::STAGES>);
+}
+static_assert(smem_bytes<GeoPrefill>() <= 232448, "MX GEMM exceeds the 227 KB shared-memory limit");
 
 struct Args {
     void* out;               // gate/up: h codes uint8 [rows, I]; down: y_perm fp32 [rows, H]
@@ -119,15 +141,17 @@ struct Pipe {
 };
 
 // tiles this CTA takes in the current phase (tile_start built)
-__device__ __forceinline__ int tiles_of_cta(const Ctl& c, int n) {
+template <class C>
+__device__ __forceinline__ int tiles_of_cta(const C& c, int n) {
     const int total = c.tile_start[n];
     return total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
 }
 
 __device__ __forceinline__ uint32_t ring_base(uint8_t* raw) { return (smem_u32(raw) + 1023u) & ~1023u; }
-__device__ __forceinline__ Ctl& ctl_of(uint8_t* raw) {
+template <class G>
+__device__ __forceinline__ Ctl<G::STAGES>& ctl_of(uint8_t* raw) {
     const uint32_t b = ring_base(raw);
-    return *reinterpret_cast<Ctl*>(raw + (b - smem_u32(raw)) + (size_t)STAGES * STAGE_BYTES);
+    return *reinterpret_cast<Ctl<G::STAGES>*>(raw + (b - smem_u32(raw)) + (size_t)G::STAGES * G::STAGE_BYTES);
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B, UE8M0 scales:
@@ -187,10 +211,11 @@ __device__ __forceinline__ uint32_t mx_quantize32(const float (&v)[32], uint32_t
 
 // `stall` > 0 (a testing hook) makes stage 0's `full` barrier wait for arrivals
 // that never come, so the MMA warp's bounded wait runs out.
-__device__ __forceinline__ void init(Ctl& c, int stall = 0) {
+template <int S>
+__device__ __forceinline__ void init(Ctl<S>& c, int stall = 0) {
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&c.full[s]), 2 + (s == 0 ? stall : 0));
             mbar_init(smem_u32(&c.empty[s]), 1);
         }
@@ -208,15 +233,16 @@ __device__ __forceinline__ void init(Ctl& c, int stall = 0) {
     }
 }
 
-// warp 0: tile_start from row_off
-__device__ __forceinline__ void build_tile_table(Ctl& c, int n, int ntiles_n) {
+// warp 0: tile_start from row_off (m-tiles of G::AR token rows)
+template <class G>
+__device__ __forceinline__ void build_tile_table(Ctl<G::STAGES>& c, int n, int ntiles_n) {
     if ((threadIdx.x >> 5) != 0) return;
     const int lane = threadIdx.x & 31;
     int carry = 0;
     for (int b0 = 0; b0 < n; b0 += 32) {
         const int e = b0 + lane;
         int v = 0;
-        if (e < n) v = ((c.row_off[e + 1] - c.row_off[e] + BM - 1) / BM) * ntiles_n;
+        if (e < n) v = ((c.row_off[e + 1] - c.row_off[e] + G::AR - 1) / G::AR) * ntiles_n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, v, o);
@@ -228,13 +254,14 @@ __device__ __forceinline__ void build_tile_table(Ctl& c, int n, int ntiles_n) {
     if (lane == 0) c.tile_start[0] = 0;
 }
 
-__device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_hint, TileCoord& tc) {
+template <class G>
+__device__ __forceinline__ bool next_tile(const Ctl<G::STAGES>& c, int n, int tile, int& e_hint, TileCoord& tc) {
     if (tile >= c.tile_start[n]) return false;
     int e = e_hint;
     while (c.tile_start[e + 1] <= tile) ++e;
     e_hint = e;
     const int cnt = c.row_off[e + 1] - c.row_off[e];
-    const int mtiles = (cnt + BM - 1) / BM;
+    const int mtiles = (cnt + G::AR - 1) / G::AR;
     const int local = tile - c.tile_start[e];
     tc.e = e;
     tc.nt = local / mtiles;
@@ -249,10 +276,11 @@ __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_
 //   reads 128 rows and the stale ones only feed output rows that are not stored);
 //   tmB0 / tmB1: weight codes with
 //   boxes of n_step rows (gate/up: W_gate / W_up) or BN rows (down: W_down twice)
-template <int MODE>
-__device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUtensorMap* tmA,
+template <int MODE, class G>
+__device__ __forceinline__ void run(Ctl<G::STAGES>& c, uint32_t ring, Pipe& pipe, const CUtensorMap* tmA,
                                     const CUtensorMap* tmB0, const CUtensorMap* tmB1, const Args& args,
                                     const CUtensorMap* tmA_small = nullptr) {
+    constexpr int STAGES = G::STAGES, STAGE_BYTES = G::STAGE_BYTES, A_BYTES = G::A_BYTES, AR = G::AR;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = args.n;
     volatile int* abort_flag = &c.abort_flag;
@@ -269,12 +297,13 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUt
         const uint64_t pol = l2_policy_evict_last();
         int g = pipe.g;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile(c, n, tile, e_hint, tc);
+        for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile<G>(c, n, tile, e_hint, tc);
              tile += gridDim.x) {
-            const int a_row = c.row_off[tc.e] + tc.mt * BM;
-            const bool small = tmA_small != nullptr && tc.cnt - tc.mt * BM <= args.a_small;
+            const int a_row = c.row_off[tc.e] + tc.mt * AR;
+            // 128-row m-tiles with few rows load only a small box of tokens
+            const bool small = AR == BM && tmA_small != nullptr && tc.cnt - tc.mt * BM <= args.a_small;
             const CUtensorMap* tma = small ? tmA_small : tmA;
-            const uint32_t stage_tx = (uint32_t)((small ? args.a_small : BM) * BKB + B_BYTES);
+            const uint32_t stage_tx = (uint32_t)((small ? args.a_small : AR) * BKB + B_BYTES);
             const int b_row = tc.e * args.w_rows + tc.nt * args.n_step;
             for (int kb = 0; kb < args.kblocks; ++kb, ++g) {
                 const int s = g % STAGES, r = g / STAGES;
@@ -317,7 +346,7 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUt
         const uint32_t sf_smem = smem_u32(&c.sf[0][0][0]);
         const uint32_t tmem = c.tmem_base;  // a register copy: the asm memory clobbers would reload it
         const uint64_t a_desc0 = sdesc_k_swz<128>(a_addr(0)), b_desc0 = sdesc_k_swz<128>(b_addr(0));
-        for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile(c, n, tile, e_hint, tc);
+        for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile<G>(c, n, tile, e_hint, tc);
              tile += gridDim.x, ++it) {
             const int acc = it & 1, use = it >> 1;
             if (!__all_sync(0xffffffffu, MX_PROF_WAIT(wa, mbar_wait_bounded(smem_u32(&c.tempty[acc]), (use & 1) ^ 1,
@@ -360,25 +389,24 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUt
             MX_PROF_ADD(10, it);
         }
     } else if (warp >= 6) {
-        // ================= scale-factor warps: warp 6 + j fills ring slot j =================
-        static_assert(STAGES == 4, "one scale warp per ring slot");
+        // ================= scale-factor warps: warp 6 + j fills the stages g with g % 4 == j =================
+        // (ring slot g % STAGES; with 4 stages warp 6 + j always fills slot j)
         const int j = warp - 6;
         const long long b_total = (long long)n * args.w_rows;
-        // stage g = k-block g % kblocks of this CTA's tile number g / kblocks; lane r = row r of each chunk
         // stage g (counted from this phase's first stage g0) = k-block g % kblocks of this
-        // CTA's tile number g / kblocks
+        // CTA's tile number g / kblocks; lane r = row r of each chunk
         const int g0 = pipe.g;
         auto load = [&](int gabs, uint32_t (&w)[10]) -> bool {
             const int g = gabs - g0;
             const int kb = g % args.kblocks;
-            if (!next_tile(c, n, blockIdx.x + (g / args.kblocks) * (int)gridDim.x, e_hint, tc)) return false;
-            const long long a_row = (long long)c.row_off[tc.e] + tc.mt * BM + lane;
+            if (!next_tile<G>(c, n, blockIdx.x + (g / args.kblocks) * (int)gridDim.x, e_hint, tc)) return false;
+            const long long a_row = (long long)c.row_off[tc.e] + tc.mt * AR + lane;
             const long long b_row = (long long)tc.e * args.w_rows + tc.nt * args.n_step + lane;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const long long row = a_row + 32 * i;
                 // L2-coherent loads: the fused decode kernel writes these words earlier in the launch
-                w[i] = row < args.a_rows ? __ldcg(args.a_s + row * args.kblocks + kb) : 0u;
+                w[i] = (32 * i < AR && row < args.a_rows) ? __ldcg(args.a_s + row * args.kblocks + kb) : 0u;
             }
 #pragma unroll
             for (int i = 0; i < 6; ++i) {
@@ -398,28 +426,28 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUt
         long long wsf = 0, tsf = clock64();
         (void)wsf;
         (void)tsf;
-        // two items in flight: the words of this slot's next stage and of the one after
-        // it are loaded before the warp waits for the slot to free up
+        // two items in flight: the words of this warp's next stage and of the one after
+        // it are loaded before the warp waits for that stage's slot to free up
         uint32_t w[10], wn[10];
-        const int gj = g0 + (((j - g0) % STAGES) + STAGES) % STAGES;  // first stage of slot j in this phase
+        const int gj = g0 + (((j - g0) % SCALE_WARPS) + SCALE_WARPS) % SCALE_WARPS;  // this warp's first stage
         bool have = load(gj, w);
-        bool have_n = have && load(gj + STAGES, wn);
-        for (int g = gj; have && !*abort_flag; g += STAGES) {
-            const int r = g / STAGES;
+        bool have_n = have && load(gj + SCALE_WARPS, wn);
+        for (int g = gj; have && !*abort_flag; g += SCALE_WARPS) {
+            const int sl = g % STAGES, r = g / STAGES;
             // the copies of this slot's previous round have completed with its MMAs
-            if (!MX_PROF_WAIT(wsf, mbar_wait_bounded(smem_u32(&c.empty[j]), (r & 1) ^ 1, abort_flag, args.status,
+            if (!MX_PROF_WAIT(wsf, mbar_wait_bounded(smem_u32(&c.empty[sl]), (r & 1) ^ 1, abort_flag, args.status,
                                                      WAIT_LIMIT)))
                 break;
-            c.sf[j][0][lane] = make_uint4(w[0], w[1], w[2], w[3]);
-            c.sf[j][1][lane] = make_uint4(w[4], w[5], w[6], w[7]);
-            c.sf[j][2][lane] = make_uint4(w[8], w[9], 0u, 0u);
+            c.sf[sl][0][lane] = make_uint4(w[0], w[1], w[2], w[3]);
+            c.sf[sl][1][lane] = make_uint4(w[4], w[5], w[6], w[7]);
+            c.sf[sl][2][lane] = make_uint4(w[8], w[9], 0u, 0u);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by tcgen05.cp (async proxy)
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&c.full[j]));
+            if (lane == 0) mbar_arrive(smem_u32(&c.full[sl]));
 #pragma unroll
             for (int i = 0; i < 10; ++i) w[i] = wn[i];
             have = have_n;
-            if (have_n) have_n = load(g + 2 * STAGES, wn);
+            if (have_n) have_n = load(g + 2 * SCALE_WARPS, wn);
         }
         if (lane == 0) {
             MX_PROF_ADD(8, wsf);
@@ -432,17 +460,19 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUt
         (void)wt;
         (void)t0;
         int it = pipe.it;
-        for (int tile = blockIdx.x; !*abort_flag && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x, ++it) {
+        for (int tile = blockIdx.x; !*abort_flag && next_tile<G>(c, n, tile, e_hint, tc); tile += gridDim.x, ++it) {
             const int acc = it & 1, use = it >> 1;
             if (!MX_PROF_WAIT(wt, mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status,
                                                     WAIT_LIMIT)))
                 break;
             tc_fence_after();
-            const int row0_in_e = tc.mt * BM + q * 32;
+            const int row0_in_e = tc.mt * AR + q * 32;
             const long long grow0 = (long long)c.row_off[tc.e] + row0_in_e;
             const uint32_t taddr = c.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             const int col0 = tc.nt * args.n_step;
-            if (MODE == MODE_GATEUP) {
+            if (q * 32 >= AR) {
+                // accumulator rows past the m-tile (AR = 32): computed from stale A rows, not stored
+            } else if (MODE == MODE_GATEUP) {
                 // thread = one token row; 32 h columns per chunk = one MX block
                 uint8_t* hq = static_cast<uint8_t*>(args.out);
                 const bool row_ok = row0_in_e + lane < tc.cnt;
@@ -516,7 +546,8 @@ __device__ __forceinline__ void run(Ctl& c, uint32_t ring, Pipe& pipe, const CUt
 }
 
 // Every thread: its counters after a phase that ran to completion.
-__device__ __forceinline__ void pipe_advance(const Ctl& c, Pipe& p, int n, int kblocks) {
+template <class C>
+__device__ __forceinline__ void pipe_advance(const C& c, Pipe& p, int n, int kblocks) {
     const int nt = tiles_of_cta(c, n);
     p.g += nt * kblocks;
     p.it += nt;
@@ -525,7 +556,8 @@ __device__ __forceinline__ void pipe_advance(const Ctl& c, Pipe& p, int n, int k
 // After a __syncthreads: drain the MMAs (bounded), free TMEM.  Every load the
 // producer issued was consumed by an MMA unless a wait gave up; then the loads
 // still land within the bounded drain below.
-__device__ __forceinline__ void teardown(Ctl& c, int32_t* status) {
+template <class C>
+__device__ __forceinline__ void teardown(C& c, int32_t* status) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 1) {
         // the lane that issued the MMAs (elect_one() of the converged warp) commits the drain

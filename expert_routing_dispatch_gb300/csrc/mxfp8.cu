@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
                           const mx::Args args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t ring = mx::ring_base(smem_raw);
-    mx::Ctl& c = mx::ctl_of(smem_raw);
+    auto& c = mx::ctl_of<mx::GeoPrefill>(smem_raw);
     const int n = args.n;
     mx::init(c, args.stall);
     if (threadIdx.x == 0) {
@@ -85,12 +85,12 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
     }
     for (int i = threadIdx.x; i <= n; i += mx::NUM_THREADS) c.row_off[i] = __ldg(offsets + i);
     __syncthreads();
-    mx::build_tile_table(c, n, args.ntiles_n);
+    mx::build_tile_table<mx::GeoPrefill>(c, n, args.ntiles_n);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     mx::Pipe pipe{0, 0};
-    mx::run<MODE>(c, ring, pipe, &tmA, &tmB0, &tmB1, args);
+    mx::run<MODE, mx::GeoPrefill>(c, ring, pipe, &tmA, &tmB0, &tmB1, args);
     __syncthreads();
     mx::teardown(c, args.status);
 }
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
 //   core (grouped_gemm_mx.cuh) keeps its ring and accumulator counters across P2
 //   and P3.  sync[0] (arrivals) and sync[1] (abort) are zero at launch.
 constexpr long long MX_GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
-constexpr int MX_SMALL_ROWS = 32;                     // rows of the small token-tile boxes
+constexpr int MX_SMALL_ROWS = 32;                     // token rows of the fused launch's m-tiles and boxes
 
 struct MxFusedArgs {
     const float* logits;
@@ -137,7 +137,7 @@ struct MxFusedSmem {
     CombineSmem comb;
     int ok;
 };
-constexpr size_t MX_FUSED_SMEM_BYTES = mx::SMEM_BYTES + sizeof(MxFusedSmem);
+constexpr size_t MX_FUSED_SMEM_BYTES = mx::smem_bytes<mx::GeoDecode>() + sizeof(MxFusedSmem);
 static_assert(MX_FUSED_SMEM_BYTES <= 232448, "fused MXFP8 kernel exceeds the 227 KB shared-memory limit");
 
 __device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
@@ -177,26 +177,25 @@ __device__ bool mx_grid_sync(const MxFusedArgs& a, unsigned target, MxFusedSmem&
 }
 
 __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
-    moe_layer_mx_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
-                              const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
+    moe_layer_mx_fused_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmU,
                               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmXs,
                               const __grid_constant__ CUtensorMap tmHs, const MxFusedArgs a) {
-    // tmXs / tmHs: the x and h codes with MX_SMALL_ROWS-row boxes, for m-tiles with that
-    // few rows (decode has ~16 rows per expert: a quarter of the token-tile bytes)
+    // tmXs / tmHs: the x and h codes with MX_SMALL_ROWS-row boxes, the m-tiles of the
+    // decode ring geometry (decode has ~16 rows per expert)
+    using GD = mx::GeoDecode;
+    static_assert(GD::AR == MX_SMALL_ROWS, "token boxes are the decode m-tiles");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t ring = mx::ring_base(smem_raw);
-    mx::Ctl& c = mx::ctl_of(smem_raw);
-    MxFusedSmem& fs = *reinterpret_cast<MxFusedSmem*>(reinterpret_cast<uint8_t*>(&c) + sizeof(mx::Ctl));
+    auto& c = mx::ctl_of<GD>(smem_raw);
+    MxFusedSmem& fs = *reinterpret_cast<MxFusedSmem*>(reinterpret_cast<uint8_t*>(&c) + sizeof(c));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = a.e1 - a.e0, T = a.T, k = a.k;
     const unsigned G = gridDim.x;
 
     mx::init(c, 0);
     if (threadIdx.x == 0) {
-        tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmG);
         tma_prefetch_desc(&tmU);
-        tma_prefetch_desc(&tmH);
         tma_prefetch_desc(&tmD);
         tma_prefetch_desc(&tmXs);
         tma_prefetch_desc(&tmHs);
@@ -337,10 +336,10 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
                           a.I,
                           mx::BN / 2,
                           0,
-                          MX_SMALL_ROWS};
-        mx::build_tile_table(c, n, nt);
+                          0};
+        mx::build_tile_table<GD>(c, n, nt);
         __syncthreads();
-        mx::run<mx::MODE_GATEUP>(c, ring, pipe, &tmX, &tmG, &tmU, ga, &tmXs);
+        mx::run<mx::MODE_GATEUP, GD>(c, ring, pipe, &tmXs, &tmG, &tmU, ga);
         mx::pipe_advance(c, pipe, n, ga.kblocks);
         ok = mx_grid_sync(a, 3u * G, fs) && !c.abort_flag;
     }
@@ -362,10 +361,10 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
                           a.H,
                           mx::BN,
                           0,
-                          MX_SMALL_ROWS};
-        mx::build_tile_table(c, n, nt);
+                          0};
+        mx::build_tile_table<GD>(c, n, nt);
         __syncthreads();
-        mx::run<mx::MODE_DOWN>(c, ring, pipe, &tmH, &tmD, &tmD, da, &tmHs);
+        mx::run<mx::MODE_DOWN, GD>(c, ring, pipe, &tmHs, &tmD, &tmD, da);
         mx::pipe_advance(c, pipe, n, da.kblocks);
         ok = mx_grid_sync(a, 4u * G, fs) && !c.abort_flag;
     }
@@ -416,9 +415,11 @@ template <int MODE>
 cudaError_t launch_mx_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                            const int32_t* offsets, const mx::Args& args, cudaStream_t s) {
     const cudaError_t attr =
-        ensure_dynamic_smem(reinterpret_cast<const void*>(&grouped_ffn_mx_kernel<MODE>), (int)mx::SMEM_BYTES);
+        ensure_dynamic_smem(reinterpret_cast<const void*>(&grouped_ffn_mx_kernel<MODE>),
+                            (int)mx::smem_bytes<mx::GeoPrefill>());
     if (attr != cudaSuccess) return attr;
-    grouped_ffn_mx_kernel<MODE><<<sm_count(), mx::NUM_THREADS, mx::SMEM_BYTES, s>>>(a, b0, b1, offsets, args);
+    grouped_ffn_mx_kernel<MODE>
+        <<<sm_count(), mx::NUM_THREADS, mx::smem_bytes<mx::GeoPrefill>(), s>>>(a, b0, b1, offsets, args);
     return cudaGetLastError();
 }
 
@@ -437,9 +438,9 @@ cudaError_t launch_layer_mx_fused(const uint16_t* x, const float* logits, const 
     if (attr != cudaSuccess) return attr;
     const int n = e1 - e0;
     const long long rows = (long long)T * k;
-    CUtensorMap mX, mG, mU, mH, mD, mXs, mHs;
-    if (!make_tmap_u8(&mX, xpq, rows, H, mx::BM) || !make_tmap_u8(&mG, wgq, (long long)n * I, H, mx::BN / 2) ||
-        !make_tmap_u8(&mU, wuq, (long long)n * I, H, mx::BN / 2) || !make_tmap_u8(&mH, hq, rows, I, mx::BM) ||
+    CUtensorMap mG, mU, mD, mXs, mHs;
+    if (!make_tmap_u8(&mG, wgq, (long long)n * I, H, mx::BN / 2) ||
+        !make_tmap_u8(&mU, wuq, (long long)n * I, H, mx::BN / 2) ||
         !make_tmap_u8(&mD, wdq, (long long)n * H, I, mx::BN) || !make_tmap_u8(&mXs, xpq, rows, H, MX_SMALL_ROWS) ||
         !make_tmap_u8(&mHs, hq, rows, I, MX_SMALL_ROWS))
         return cudaErrorInvalidValue;
@@ -457,7 +458,7 @@ cudaError_t launch_layer_mx_fused(const uint16_t* x, const float* logits, const 
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_layer_mx_fused_kernel, mX, mG, mU, mH, mD, mXs, mHs, a);
+    return cudaLaunchKernelEx(&cfg, moe_layer_mx_fused_kernel, mG, mU, mD, mXs, mHs, a);
 }
 
 cudaError_t launch_mx_quantize(const uint16_t* src, long long rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st) {
