@@ -37,7 +37,8 @@ namespace {
 using namespace gemm;
 
 constexpr long long GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles
-constexpr int SMALL_ROWS = 32;                    // rows of the small token-tile boxes
+constexpr int SMALL_ROWS = 32;                    // token rows of the m-tiles and their boxes
+static_assert(SMALL_ROWS == AR, "token boxes are the GEMM core's m-tiles");
 
 struct FusedArgs {
     const float* logits;
@@ -107,12 +108,11 @@ __device__ bool grid_sync(const FusedArgs& a, unsigned target, FusedSmem& fs) {
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    moe_layer_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ WMaps wmGU,
-                           const __grid_constant__ CUtensorMap tmH, const __grid_constant__ WMaps wmD,
+    moe_layer_fused_kernel(const __grid_constant__ WMaps wmGU, const __grid_constant__ WMaps wmD,
                            const __grid_constant__ CUtensorMap tmXs, const __grid_constant__ CUtensorMap tmHs,
                            const FusedArgs a) {
-    // tmXs / tmHs: x_perm / h with SMALL_ROWS-row boxes, for m-tiles with that few rows
-    // (decode has ~16 tokens per expert: 4x less token-tile traffic than 128-row boxes)
+    // tmXs / tmHs: x_perm / h with SMALL_ROWS-row boxes, the m-tiles of the GEMM core
+    // (decode has ~16 tokens per expert)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t ring = ring_base(smem_raw);
     Ctl& c = ctl_of(smem_raw);
@@ -124,8 +124,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     init(c);
     if (threadIdx.x == 0) {
-        tma_prefetch_desc(&tmX);
-        tma_prefetch_desc(&tmH);
         tma_prefetch_desc(&tmXs);
         tma_prefetch_desc(&tmHs);
         for (int i = 0; i < 3; ++i) {
@@ -239,22 +237,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // ---------------- P2: gate/up GEMM + SiLU*up
     if (ok) {
-        const Args ga{a.h, a.status, n, a.H / BK, (a.I + a.bn / 2 - 1) / (a.bn / 2), a.I, a.I, a.bn / 2, a.bn,
-                      SMALL_ROWS, 0, 0};
+        const Args ga{a.h, a.status, n, a.H / BK, (a.I + a.bn / 2 - 1) / (a.bn / 2), a.I, a.I, a.bn / 2, a.bn, 0, 0};
         build_tile_table(c, n, ga.ntiles_n, ga.bn);
         __syncthreads();
-        run_phase<MODE_GATEUP>(c, ring, p, &tmX, &wmGU, ga, &tmXs);
+        run_phase<MODE_GATEUP>(c, ring, p, &tmXs, &wmGU, ga);
         ok = grid_sync(a, 3u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }
 
     // ---------------- P3: down GEMM
     if (ok) {
         // K = 2 I: h as hi and lo terms, each pair of k-blocks against one weight k-block
-        const Args da{a.y_perm, a.status, n, 2 * a.I / BK, (a.H + a.bn - 1) / a.bn, a.H, a.H, a.bn, a.bn, SMALL_ROWS,
-                      1, 0};
+        const Args da{a.y_perm, a.status, n, 2 * a.I / BK, (a.H + a.bn - 1) / a.bn, a.H, a.H, a.bn, a.bn, 1, 0};
         build_tile_table(c, n, da.ntiles_n, da.bn);
         __syncthreads();
-        run_phase<MODE_DOWN>(c, ring, p, &tmH, &wmD, da, &tmHs);
+        run_phase<MODE_DOWN>(c, ring, p, &tmHs, &wmD, da);
         ok = grid_sync(a, 4u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }
 
@@ -287,11 +283,11 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     // each tile then reloads its token tile for half the work.)
     const int grid = sm_count();
     const int bn = BN;
-    CUtensorMap mX, mH, mXs, mHs;
+    CUtensorMap mXs, mHs;
     WMaps wGU, wD;
     if (!make_tmap_bf16(&mXs, x_perm, rows, H, SMALL_ROWS) || !make_tmap_bf16(&mHs, h, rows, 2 * I, SMALL_ROWS) ||
-        !make_tmap_bf16(&mX, x_perm, rows, H, BM) || !make_wmaps(&wGU, w_gate, w_up, (long long)n * I, H, bn / 2) ||
-        !make_tmap_bf16(&mH, h, rows, 2 * I, BM) || !make_wmaps(&wD, w_down, nullptr, (long long)n * H, I, bn))
+        !make_wmaps(&wGU, w_gate, w_up, (long long)n * I, H, bn / 2) ||
+        !make_wmaps(&wD, w_down, nullptr, (long long)n * H, I, bn))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
@@ -308,7 +304,7 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_layer_fused_kernel, mX, wGU, mH, wD, mXs, mHs, a);
+    return cudaLaunchKernelEx(&cfg, moe_layer_fused_kernel, wGU, wD, mXs, mHs, a);
 }
 
 }  // namespace moe

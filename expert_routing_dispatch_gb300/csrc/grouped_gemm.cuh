@@ -13,15 +13,18 @@
 //   down    : acc[128 x 256] = h[rows] . W_down[e][n..n+255]^T over K = 2 I: the
 //             k-blocks alternate hi and lo of h against the same weight k-block,
 //             so y_perm = W_down (hi + lo) (fp32)
-// Tiles are (expert, m-tile of 128 rows, n-tile); the tile table is built on
-// the device from the row offsets.  Within an expert the m-tiles of one n-tile
+// Tiles are (expert, m-tile of 32 rows, n-tile); the tile table is built on
+// the device from the row offsets.  Decode has ~16 rows per expert, so a stage
+// carries 32 token rows (4 KB) next to its 256 weight rows; the MMA keeps M = 128,
+// its A rows 32..127 read the bytes after the token slot (inside the ring) and
+// only feed accumulator rows that are never stored.  Within an expert the m-tiles of one n-tile
 // are consecutive, so CTAs running side by side share a weight tile through L2.
 // When the last round of tiles would leave most CTAs idle (r tiles, 2r or 4r <=
 // CTAs), each of those r tiles is split along N into 2 or 4 pieces (narrower
 // MMA N, weight boxes and epilogue), which spreads the last round over more SMs.
 //
-// CTA = 6 warps: warp 0 issues TMA loads (128-byte swizzle) into a 4-stage
-// shared-memory ring; warp 1 owns 512 TMEM columns (two 256-column fp32
+// CTA = 6 warps: warp 0 issues TMA loads (128-byte swizzle) into a 5-stage
+// shared-memory ring (160 KB of weights in flight); warp 1 owns 512 TMEM columns (two 256-column fp32
 // accumulators) and issues tcgen05.mma (M=128, N=256, K=16) from one elected
 // lane while all 32 lanes run the loop; warps 2..5 drain TMEM with tcgen05.ld
 // and run the epilogue while the next tile accumulates into the other buffer.
@@ -34,10 +37,11 @@
 namespace moe {
 namespace gemm {
 
-// Tile shape: BK = 64 bf16 (128-byte rows, 128-byte swizzle), 4 ring stages.
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int ROW_BYTES = BK * 2;  // bytes of one K-row of a tile = swizzle span
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+// MMA shape M = BM, N = BN; BK = 64 bf16 (128-byte rows, 128-byte swizzle);
+// m-tiles of AR token rows; 5 ring stages.
+constexpr int BM = 128, BN = 256, BK = 64, AR = 32, STAGES = 5;
+constexpr int ROW_BYTES = BK * 2;     // bytes of one K-row of a tile = swizzle span
+constexpr int A_BYTES = AR * BK * 2;  // 4 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
@@ -76,7 +80,6 @@ struct Args {
     int b_rows;       // weight rows per expert in the B tensor map (I or H)
     int n_step;       // output columns per n-tile (bn / 2 for gate/up, bn for down)
     int bn;           // MMA N = weight rows per tile (256; 128 also supported)
-    int a_small;      // box rows of the optional small token map (0 = none)
     int ksplit;       // weight k-block of token k-block kb: kb >> ksplit (1 for down: hi and lo share it)
     int stall;        // testing hook: extra arrivals ring stage 0 waits for (0 in normal use)
 };
@@ -148,7 +151,7 @@ __device__ __forceinline__ void build_tile_table(Ctl& c, int n, int ntiles_n, in
     for (int b0 = 0; b0 < n; b0 += 32) {
         const int e = b0 + lane;
         int v = 0;
-        if (e < n) v = ((c.row_off[e + 1] - c.row_off[e] + BM - 1) / BM) * ntiles_n;
+        if (e < n) v = ((c.row_off[e + 1] - c.row_off[e] + AR - 1) / AR) * ntiles_n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, v, o);
@@ -186,7 +189,7 @@ __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_
     while (c.tile_start[e + 1] <= f) ++e;  // tiles increase monotonically per CTA
     e_hint = e;
     const int cnt = c.row_off[e + 1] - c.row_off[e];
-    const int mtiles = (cnt + BM - 1) / BM;
+    const int mtiles = (cnt + AR - 1) / AR;
     const int local = f - c.tile_start[e];
     tc.e = e;
     tc.nt = local / mtiles;
@@ -196,12 +199,10 @@ __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_
 }
 
 // One GEMM phase, every thread of the CTA calls it and plays its role.
-//   tmA_small (optional): the same token matrix with args.a_small-row boxes.  An
-//   m-tile with at most a_small valid rows loads only those rows; the MMA still
-//   reads 128 rows, and the stale ones only feed output rows that are not stored.
+//   tmA: the token matrix with AR-row boxes.
 template <int MODE>
 __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const CUtensorMap* tmA, const WMaps* wm,
-                                          const Args& args, const CUtensorMap* tmA_small = nullptr) {
+                                          const Args& args) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = args.n;
     volatile int* abort_flag = &c.abort_flag;
@@ -216,15 +217,14 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
         TileCoord tc;
         bool ok = !__any_sync(0xffffffffu, *abort_flag);
         for (int tile = blockIdx.x; ok && next_tile(c, n, tile, e_hint, tc); tile += gridDim.x) {
-            const int a_row = c.row_off[tc.e] + tc.mt * BM;
+            const int a_row = c.row_off[tc.e] + tc.mt * AR;
             const int piece_rows = args.n_step >> tc.shift;  // weight rows of one map's box
             const int b_row = tc.e * args.b_rows + tc.nt * args.n_step + tc.piece * piece_rows;
             const int bn_t = args.bn >> tc.shift;
             const CUtensorMap* tmB0 = &wm->b0[tc.shift];
             const CUtensorMap* tmB1 = &wm->b1[tc.shift];
-            const bool a_small = tmA_small != nullptr && tc.cnt - tc.mt * BM <= args.a_small;
-            const CUtensorMap* tma_a = a_small ? tmA_small : tmA;
-            const uint32_t stage_tx = (uint32_t)((a_small ? args.a_small : BM) * BK * 2 + bn_t * BK * 2);
+            const CUtensorMap* tma_a = tmA;
+            const uint32_t stage_tx = (uint32_t)(AR * BK * 2 + bn_t * BK * 2);
             for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                 const int s = p.g % STAGES, r = p.g / STAGES;
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
@@ -298,13 +298,15 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             const int acc = p.it & 1, use = p.it >> 1;
             if (!mbar_wait_bounded(smem_u32(&c.tfull[acc]), use & 1, abort_flag, args.status, WAIT_LIMIT)) break;
             tc_fence_after();
-            const int row0_in_e = tc.mt * BM + q * 32;  // first row of this warp's block
+            const int row0_in_e = tc.mt * AR + q * 32;  // first row of this warp's block
             const long long grow0 = (long long)c.row_off[tc.e] + row0_in_e;
             const uint32_t taddr = c.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const int bn_t = args.bn >> tc.shift;
             const int col0 = tc.nt * args.n_step + tc.piece * (args.n_step >> tc.shift);
             uint4* st = c.stage[q];
-            if (MODE == MODE_GATEUP) {
+            if (q * 32 >= AR) {
+                // accumulator rows past the m-tile: computed from stale A rows, not stored
+            } else if (MODE == MODE_GATEUP) {
                 // 32 h columns per chunk (one half of a 64-column block of the split layout):
                 // 64 B of hi and 64 B of lo per row, each staged as 4 slots; slot = piece ^ ((row >> 1) & 3)
                 uint16_t* out = static_cast<uint16_t*>(args.out);
