@@ -62,6 +62,9 @@ def parse():
     p.add_argument("--precision", choices=["bf16", "mxfp8"], default="bf16",
                    help="expert GEMM operands: bf16 (the workload's statement), or MXFP8 expert weights and "
                         "activations (moe_layer_mxfp8; weights quantised on the device before timing)")
+    p.add_argument("--dispatch", choices=["copy", "gather"], default="copy",
+                   help="copy: dispatch stages the token rows in x_perm (moe_layer); gather: the gate/up GEMM "
+                        "gathers them from x by TMA (moe_layer_gather, decode-sized bf16 workloads only)")
     return p.parse_args()
 
 
@@ -382,11 +385,16 @@ def run_ours(args):
     else:
         lws = moe.alloc_workspace(moe.moe_workspace_size(dims), dev)
 
+    gather = args.dispatch == "gather"
+    if gather and (mx or P > moe.FUSED_MAX_PAIRS):
+        raise SystemExit("--dispatch gather: bf16 decode-sized workloads only (T*k <= %d)" % moe.FUSED_MAX_PAIRS)
+    layer_fn = moe.moe_layer_gather if gather else moe.moe_layer
+
     def run_layer(x_, lg_, out_, **kw):
         if mx:
             moe.moe_layer_mxfp8(dims, x_, lg_, wq["g"], wq["u"], wq["d"], out_, lws, status=status, stream=sh, **kw)
         else:
-            moe.moe_layer(dims, x_, lg_, wg, wu, wd, out_, lws, status=status, stream=sh, **kw)
+            layer_fn(dims, x_, lg_, wg, wu, wd, out_, lws, status=status, stream=sh, **kw)
 
     fused = P <= moe.FUSED_MAX_PAIRS and not mx
     mx_fused = P <= moe.FUSED_MAX_PAIRS and mx
@@ -646,13 +654,15 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "mxfp8 (e4m3, ue8m0 block-32 scales; fp32 accumulate)" if mx else "bf16",
         "data": "synthetic (seeded counter-based generator; random-init weights)",
-        "config": dict(workload_config(cfg, R), **({"precision": "mxfp8"} if mx else {})),
+        "config": dict(workload_config(cfg, R), **({"precision": "mxfp8"} if mx else {}),
+                       **({"dispatch": "tma_row_gather"} if gather else {})),
         "e2e": {"value": job_throughput(world, T, t_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(inp["x"].nbytes + inp["logits"].nbytes),
                 "d2h_bytes_per_step": int(T * H * 4),
                 "ms_per_step": t_e2e,
                 "serial_value": job_throughput(world, T, t_e2e_serial), "serial_ms_per_step": t_e2e_serial,
-                "note": ("moe_layer per step with its pinned-host x/logits upload and fp32 output download; "
+                "note": (("moe_layer_mxfp8" if mx else layer_fn.__name__) +
+                         " per step with its pinned-host x/logits upload and fp32 output download; "
                          "value: uploads, layers and downloads of consecutive steps pipelined on 3 streams "
                          "(double-buffered); serial_value: copies and layer back to back, L2 flushed; "
                          "expert weights resident")},

@@ -12,7 +12,7 @@ import os
 
 __all__ = [
     "MoeError", "Dims", "lib", "build", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine",
-    "moe_layer", "moe_combine_accumulate", "moe_expert_gate_up", "moe_expert_down", "moe_workspace_size", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
+    "moe_layer", "moe_layer_gather", "moe_combine_accumulate", "moe_expert_gate_up", "moe_expert_down", "moe_workspace_size", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
     "moe_status_string", "alloc_workspace", "EXPORTED", "moe_testing_layer_stalled_barrier", "FUSED_MAX_PAIRS",
     "moe_quantize_mxfp8", "moe_expert_ffn_mxfp8_workspace_size", "moe_expert_ffn_mxfp8", "moe_layer_mxfp8_workspace_size",
     "moe_layer_mxfp8", "moe_testing_expert_gate_up_stalled", "moe_testing_expert_ffn_mxfp8_stalled",
@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmoe.so")
 # every symbol include/moe.h declares
 EXPORTED = ("moe_status_string", "moe_dispatch_workspace_size", "moe_expert_ffn_workspace_size",
             "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_expert_gate_up",
-            "moe_expert_down", "moe_combine", "moe_combine_accumulate", "moe_layer",
+            "moe_expert_down", "moe_combine", "moe_combine_accumulate", "moe_layer", "moe_layer_gather",
             "moe_testing_layer_stalled_barrier", "moe_quantize_mxfp8", "moe_expert_ffn_mxfp8_workspace_size",
             "moe_expert_ffn_mxfp8", "moe_layer_mxfp8_workspace_size", "moe_layer_mxfp8",
             "moe_testing_expert_gate_up_stalled", "moe_testing_expert_ffn_mxfp8_stalled")
@@ -89,13 +89,15 @@ def lib():
         L.moe_combine.argtypes = [pd, vp, vp, vp, vp, vp]
         L.moe_combine_accumulate.argtypes = [pd, vp, vp, vp, vp, vp]
         L.moe_layer.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+        L.moe_layer_gather.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         L.moe_testing_layer_stalled_barrier.argtypes = [pd, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         L.moe_quantize_mxfp8.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, vp, vp, vp]
         L.moe_expert_ffn_mxfp8.argtypes = [pd] + [vp] * 11 + [sz, vp, vp]
         L.moe_testing_expert_ffn_mxfp8_stalled.argtypes = [pd] + [vp] * 11 + [sz, vp, vp]
         L.moe_layer_mxfp8.argtypes = [pd] + [vp] * 12 + [sz, vp, vp]
         for f in (L.moe_route, L.moe_dispatch, L.moe_dispatch_noalloc, L.moe_expert_ffn, L.moe_expert_gate_up, L.moe_expert_down,
-                  L.moe_combine, L.moe_combine_accumulate, L.moe_layer, L.moe_testing_layer_stalled_barrier,
+                  L.moe_combine, L.moe_combine_accumulate, L.moe_layer, L.moe_layer_gather,
+                  L.moe_testing_layer_stalled_barrier,
                   L.moe_quantize_mxfp8, L.moe_expert_ffn_mxfp8, L.moe_layer_mxfp8,
                   L.moe_testing_expert_gate_up_stalled, L.moe_testing_expert_ffn_mxfp8_stalled):
             f.restype = i32
@@ -226,6 +228,16 @@ def moe_layer(dims, x, logits, w_gate, w_up, w_down, out, ws, ws_bytes=None, top
     nb = _nbytes(ws) if ws_bytes is None else ws_bytes
     _check(lib().moe_layer(ctypes.byref(d), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(out),
                            _ptr(topk_idx), _ptr(topk_w), _ptr(ws), nb, _ptr(status), _stream(stream)), "moe_layer")
+
+
+def moe_layer_gather(dims, x, logits, w_gate, w_up, w_down, out, ws, ws_bytes=None, topk_idx=None, topk_w=None,
+                     status=None, stream=None):
+    """moe_layer's fused path with the gate/up token rows gathered from x by TMA (no x_perm)."""
+    d = Dims.of(dims)
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    _check(lib().moe_layer_gather(ctypes.byref(d), _ptr(x), _ptr(logits), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                  _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), nb, _ptr(status),
+                                  _stream(stream)), "moe_layer_gather")
 
 
 def moe_testing_layer_stalled_barrier(dims, x, logits, w_gate, w_up, w_down, out, ws, ws_bytes=None, status=None,

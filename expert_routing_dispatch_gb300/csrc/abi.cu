@@ -347,7 +347,8 @@ int moe_combine_accumulate(const moe_dims* d, const float* y_perm, const int32_t
 
 static int layer_impl(const moe_dims* d, const uint16_t* x, const float* logits, const uint16_t* w_gate,
                       const uint16_t* w_up, const uint16_t* w_down, float* out, int32_t* topk_idx_opt,
-                      float* topk_w_opt, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream, int stall) {
+                      float* topk_w_opt, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream, int stall,
+                      int gather = 0) {
     int st = check_dims(d);
     if (st) return st;
     if (!aligned16(x) || !aligned16(logits) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
@@ -357,6 +358,7 @@ static int layer_impl(const moe_dims* d, const uint16_t* x, const float* logits,
         return MOE_ERR_INVALID_ARG;
     const bool fused = (long long)pairs_of(d) <= MOE_FUSED_MAX_PAIRS;
     if (stall && !fused) return MOE_ERR_INVALID_ARG;
+    if (gather && !fused) return MOE_ERR_UNSUPPORTED;
     const LayerWs need = carve(d, nullptr);
     if (!ws_ok(ws, ws_bytes, need.total)) return MOE_ERR_WORKSPACE;
     if ((st = check_device())) return st;
@@ -368,7 +370,7 @@ static int layer_impl(const moe_dims* d, const uint16_t* x, const float* logits,
         return launched(launch_layer_fused(x, logits, w_gate, w_up, w_down, out, idx, wt, w.counts, w.offsets,
                                            w.row_pair, w.pair_row, w.x_perm, static_cast<uint16_t*>(w.ffn_ws),
                                            w.y_perm, w.sync, d->T, d->H, d->I, d->E, d->k, d->e0, d->e1,
-                                           status_dev, stall, s));
+                                           status_dev, stall, s, gather));
     // route also accumulates the dispatch chunk histograms; place then needs no counting pass
     int32_t* hist = static_cast<int32_t*>(w.dispatch_ws);
     if (cudaMemsetAsync(hist, 0, w.dispatch_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -390,6 +392,13 @@ int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits, const u
               int32_t* status_dev, void* stream) {
     return layer_impl(d, x, logits, w_gate, w_up, w_down, out, topk_idx_opt, topk_w_opt, ws, ws_bytes, status_dev,
                       stream, 0);
+}
+
+int moe_layer_gather(const moe_dims* d, const uint16_t* x, const float* logits, const uint16_t* w_gate,
+                     const uint16_t* w_up, const uint16_t* w_down, float* out, int32_t* topk_idx_opt,
+                     float* topk_w_opt, void* ws, size_t ws_bytes, int32_t* status_dev, void* stream) {
+    return layer_impl(d, x, logits, w_gate, w_up, w_down, out, topk_idx_opt, topk_w_opt, ws, ws_bytes, status_dev,
+                      stream, 0, 1);
 }
 
 int moe_testing_layer_stalled_barrier(const moe_dims* d, const uint16_t* x, const float* logits,

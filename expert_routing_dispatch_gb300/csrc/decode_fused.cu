@@ -58,6 +58,7 @@ struct FusedArgs {
     int T, H, I, E, k, e0, e1;
     int bn;     // MMA N (weight rows per GEMM tile): 256, or 128 when there are few local experts
     int stall;  // testing hook: extra arrivals the first barrier waits for (0 in normal use)
+    int gather; // 1: no x_perm; the gate/up GEMM gathers its token rows from x (tile::gather4)
 };
 
 struct FusedSmem {
@@ -110,9 +111,10 @@ __device__ bool grid_sync(const FusedArgs& a, unsigned target, FusedSmem& fs) {
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     moe_layer_fused_kernel(const __grid_constant__ WMaps wmGU, const __grid_constant__ WMaps wmD,
                            const __grid_constant__ CUtensorMap tmXs, const __grid_constant__ CUtensorMap tmHs,
-                           const FusedArgs a) {
+                           const __grid_constant__ CUtensorMap tmXg, const FusedArgs a) {
     // tmXs / tmHs: x_perm / h with SMALL_ROWS-row boxes, the m-tiles of the GEMM core
-    // (decode has ~16 tokens per expert)
+    // (decode has ~16 tokens per expert); tmXg: x [T, H] with one-row boxes, the
+    // source of the gate/up token rows when a.gather is set
     extern __shared__ uint8_t smem_raw[];
     const uint32_t ring = ring_base(smem_raw);
     Ctl& c = ctl_of(smem_raw);
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     init(c);
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmXs);
+        tma_prefetch_desc(&tmXg);
         tma_prefetch_desc(&tmHs);
         for (int i = 0; i < 3; ++i) {
             tma_prefetch_desc(&wmGU.b0[i]);
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncthreads();
         const int H8 = a.H / 8;
-        for (int t = t0; t < t1; ++t) {  // copy x rows of this CTA's tokens
+        for (int t = t0; t < t1 && !a.gather; ++t) {  // copy x rows of this CTA's tokens
             if (threadIdx.x < 32) {
                 const int r = (lane < k) ? a.pair_row[(size_t)t * k + lane] : -1;
                 const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
@@ -240,7 +243,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Args ga{a.h, a.status, n, a.H / BK, (a.I + a.bn / 2 - 1) / (a.bn / 2), a.I, a.I, a.bn / 2, a.bn, 0, 0};
         build_tile_table(c, n, ga.ntiles_n, ga.bn);
         __syncthreads();
-        run_phase<MODE_GATEUP>(c, ring, p, &tmXs, &wmGU, ga);
+        if (a.gather)
+            run_phase<MODE_GATEUP>(c, ring, p, &tmXg, &wmGU, ga, a.row_pair, k);
+        else
+            run_phase<MODE_GATEUP>(c, ring, p, &tmXs, &wmGU, ga);
         ok = grid_sync(a, 3u * G + (unsigned)a.stall, fs) && !c.abort_flag;
     }
 
@@ -273,7 +279,7 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
                                int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
                                uint16_t* x_perm, uint16_t* h, float* y_perm, unsigned* sync, int T, int H, int I,
                                int E, int k, int e0, int e1, int32_t* status, int stall_first_barrier,
-                               cudaStream_t s) {
+                               cudaStream_t s, int gather) {
     const cudaError_t attr =
         ensure_dynamic_smem(reinterpret_cast<const void*>(&moe_layer_fused_kernel), (int)FUSED_SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
@@ -283,9 +289,10 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     // each tile then reloads its token tile for half the work.)
     const int grid = sm_count();
     const int bn = BN;
-    CUtensorMap mXs, mHs;
+    CUtensorMap mXs, mHs, mXg;
     WMaps wGU, wD;
     if (!make_tmap_bf16(&mXs, x_perm, rows, H, SMALL_ROWS) || !make_tmap_bf16(&mHs, h, rows, 2 * I, SMALL_ROWS) ||
+        !make_tmap_bf16(&mXg, x, T, H, 1) ||
         !make_wmaps(&wGU, w_gate, w_up, (long long)n * I, H, bn / 2) ||
         !make_wmaps(&wD, w_down, nullptr, (long long)n * H, I, bn))
         return cudaErrorInvalidValue;
@@ -293,7 +300,7 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     if (e != cudaSuccess) return e;
     FusedArgs a{logits, reinterpret_cast<const uint4*>(x), topk_idx, topk_w, counts, offsets, row_pair, pair_row,
                 reinterpret_cast<uint4*>(x_perm), h, y_perm, out, sync, status, T, H, I, E, k, e0, e1, bn,
-                stall_first_barrier};
+                stall_first_barrier, gather};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NUM_THREADS);
@@ -304,7 +311,7 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_layer_fused_kernel, wGU, wD, mXs, mHs, a);
+    return cudaLaunchKernelEx(&cfg, moe_layer_fused_kernel, wGU, wD, mXs, mHs, mXg, a);
 }
 
 }  // namespace moe

@@ -40,6 +40,7 @@ namespace gemm {
 // MMA shape M = BM, N = BN; BK = 64 bf16 (128-byte rows, 128-byte swizzle);
 // m-tiles of AR token rows; 5 ring stages.
 constexpr int BM = 128, BN = 256, BK = 64, AR = 32, STAGES = 5;
+static_assert(AR <= 32 && AR % 4 == 0, "one producer lane per m-tile row; four-row gathers");
 constexpr int ROW_BYTES = BK * 2;     // bytes of one K-row of a tile = swizzle span
 constexpr int A_BYTES = AR * BK * 2;  // 4 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
@@ -199,10 +200,14 @@ __device__ __forceinline__ bool next_tile(const Ctl& c, int n, int tile, int& e_
 }
 
 // One GEMM phase, every thread of the CTA calls it and plays its role.
-//   tmA: the token matrix with AR-row boxes.
+//   tmA: the token matrix with AR-row boxes, or (gather_pairs != NULL) the token-major
+//   x [T, H] with one-row boxes: row i of an m-tile is then x[gather_pairs[row] /
+//   gather_k], loaded by tile::gather4, four rows per copy (the grouped copy x_perm is
+//   never written).  Rows past the expert's count repeat the m-tile's first token.
 template <int MODE>
 __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const CUtensorMap* tmA, const WMaps* wm,
-                                          const Args& args) {
+                                          const Args& args, const int32_t* gather_pairs = nullptr,
+                                          int gather_k = 1) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = args.n;
     volatile int* abort_flag = &c.abort_flag;
@@ -225,6 +230,11 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             const CUtensorMap* tmB1 = &wm->b1[tc.shift];
             const CUtensorMap* tma_a = tmA;
             const uint32_t stage_tx = (uint32_t)(AR * BK * 2 + bn_t * BK * 2);
+            int tok = 0;  // gather: lane i holds the token of m-tile row i (written earlier in the launch)
+            if (gather_pairs != nullptr) {
+                const int valid = tc.cnt - tc.mt * AR;
+                tok = __ldcg(gather_pairs + a_row + (lane < valid ? lane : 0)) / gather_k;
+            }
             for (int kb = 0; kb < args.kblocks; ++kb, ++p.g) {
                 const int s = p.g % STAGES, r = p.g / STAGES;
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&c.empty[s]), (r & 1) ^ 1, abort_flag,
@@ -233,19 +243,33 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     break;
                 }
                 p.issued[s] = r + 1;
-                if (elect_one()) {
+                const bool leader = elect_one();
+                const uint32_t fb = smem_u32(&c.full[s]);
+                if (leader) {
                     // Each copy takes ~100 cycles to issue.  Gate/up issues its two weight
                     // boxes before the token box; down keeps the token box first.
-                    const uint32_t fb = smem_u32(&c.full[s]);
                     const int wk = (kb >> args.ksplit) * BK;
                     mbar_arrive_expect_tx(fb, stage_tx);
                     if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn_t/2 each
                         tma_load_2d(b_addr(s), tmB0, wk, b_row, fb, pol_b);
                         tma_load_2d(b_addr(s) + (uint32_t)(bn_t / 2) * BK * 2, tmB1, wk, b_row, fb, pol_b);
-                        tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
+                        if (gather_pairs == nullptr) tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
                     } else {
                         tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
                         tma_load_2d(b_addr(s), tmB0, wk, b_row, fb, pol_b);
+                    }
+                }
+                if (MODE == MODE_GATEUP && gather_pairs != nullptr) {
+                    // AR rows as AR / 4 four-row gathers into consecutive 512-byte row groups
+#pragma unroll
+                    for (int j = 0; j < AR / 4; ++j) {
+                        const int t0 = __shfl_sync(0xffffffffu, tok, 4 * j);
+                        const int t1 = __shfl_sync(0xffffffffu, tok, 4 * j + 1);
+                        const int t2 = __shfl_sync(0xffffffffu, tok, 4 * j + 2);
+                        const int t3 = __shfl_sync(0xffffffffu, tok, 4 * j + 3);
+                        if (leader)
+                            tma_gather4_2d(a_addr(s) + (uint32_t)(j * 4 * ROW_BYTES), tma_a, kb * BK, t0, t1, t2, t3,
+                                           fb, pol_a);
                     }
                 }
                 __syncwarp();

@@ -68,7 +68,7 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
                                int32_t* counts, int32_t* offsets, int32_t* row_pair, int32_t* pair_row,
                                uint16_t* x_perm, uint16_t* h, float* y_perm, unsigned* sync, int T, int H, int I,
                                int E, int k, int e0, int e1, int32_t* status, int stall_first_barrier,
-                               cudaStream_t s);
+                               cudaStream_t s, int gather = 0);
 
 // mxfp8.cu: the MXFP8 expert FFN (E4M3 codes, UE8M0 scales per 32 elements along K)
 cudaError_t launch_mx_quantize(const uint16_t* src, long long rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st);

@@ -225,6 +225,21 @@ int moe_layer(const moe_dims* d, const uint16_t* x, const float* logits,
               void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /*
+ * moe_layer's fused path with dispatch by TMA row gather ("Expert Parallel"
+ * section: dispatch stages the tokens routed to the local experts for the grouped
+ * GEMM).  Dispatch writes no grouped copy of x: the gate/up GEMM loads the token
+ * rows of each m-tile straight from x [T, H] into its operand tiles with
+ * tile::gather4 copies (four rows each), indexed by row_pair (token = pair / k).
+ * Same arguments, outputs and workspace as moe_layer, and bit-identical results;
+ * the x_perm part of the workspace is left unwritten.  Requires
+ * T*k <= MOE_FUSED_MAX_PAIRS (else MOE_ERR_UNSUPPORTED, nothing launched).
+ */
+int moe_layer_gather(const moe_dims* d, const uint16_t* x, const float* logits,
+                     const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                     float* out, int32_t* topk_idx_opt, float* topk_w_opt,
+                     void* ws, size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
  * Testing hook for failure detection without a GPU fault: the fused path of
  * moe_layer with its first grid-wide barrier told to wait for one CTA more than
  * the grid holds, so that wait runs out (~1 s of GPU clock cycles).  The kernel

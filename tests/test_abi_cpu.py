@@ -108,3 +108,15 @@ def test_mxfp8_entries_reject_bad_arguments_without_gpu(moe):
     assert L.moe_quantize_mxfp8(ok, -1, 64, ok, ok, None) == 1
     assert L.moe_quantize_mxfp8(ok + 2, 4, 64, ok, ok, None) == 1
     assert L.moe_quantize_mxfp8(ok, 0, 64, ok, ok, None) == 0  # nothing to do, no launch
+
+
+def test_layer_gather_rejects_split_sizes_without_gpu(moe):
+    # dispatch by TMA row gather exists on the fused path only: T*k above the fused limit is unsupported
+    L = moe.lib()
+    ok = 1 << 20
+    d = moe.Dims(moe.FUSED_MAX_PAIRS // 4 + 1, 256, 128, 16, 4, 0, 16)
+    assert L.moe_layer_gather(ctypes.byref(d), ok, ok, ok, ok, ok, ok, None, None, ok, 1 << 40, None, None) == 2
+    d = moe.Dims(64, 256, 128, 16, 4, 0, 16)
+    need = moe.moe_workspace_size(d)
+    assert L.moe_layer_gather(ctypes.byref(d), ok, ok, ok, ok, ok, ok + 2, None, None, ok, need, None, None) == 1
+    assert L.moe_layer_gather(ctypes.byref(d), ok, ok, ok, ok, ok, ok, None, None, ok, need - 1, None, None) == 3
