@@ -102,17 +102,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
         : "memory");
 }
-// Four rows r0..r3 of a 2-D tensor, columns [c0, c0 + box width), gathered into
-// four consecutive box-rows at `dst` (the map's box is one row high); completion
-// on `bar` (tx bytes)
-__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t r0, int32_t r1,
-                                               int32_t r2, int32_t r3, uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
-        : "memory");
-}
 // 2-D tiled bulk prefetch global -> L2 (no shared memory, no completion)
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -52,6 +52,19 @@ constexpr long long WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
 
+// Four rows r0..r3 of a 2-D tensor, columns [c0, c0 + box width), gathered into
+// four consecutive box-rows at `dst` (the map's box is one row high); completion
+// on `bar` (tx bytes)
+__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t r0, int32_t r1,
+                                               int32_t r2, int32_t r3, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+
 struct Ctl {
     // per epilogue warp: a 32-row x 128-byte staging tile (16-byte slots XOR-swizzled by
     // row) that turns per-row TMEM reads into whole 128-byte row segments in global memory
