@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer routed tokens/s + TFLOP/s (prefill), weight GB/s (decode), 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 NOMINAL_BF16_DENSE_TFLOPS = 2250.0  # GB300 dense bf16 tensor peak, vendor figure
+NOMINAL_FP8_DENSE_TFLOPS = 4500.0  # GB300 dense fp8 tensor peak, vendor figure
 LOAD_SECONDS = 3.0  # back-to-back steps under the clock sampler, outside the timed events
 L2_FLUSH_BYTES = 256 << 20
 _CS = "expert_routing_dispatch_gb300/csrc/"
@@ -614,6 +615,8 @@ def run_ours(args):
         roofline = {"kernel": "grouped_ffn_mx_kernel gate/up + down (tcgen05 kind::mxf8f6f4 block-scaled)",
                     "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                     "frac": achieved / fp8_peak, "peak_source": f"{peak_src} bf16 burst x 2 (nominal fp8 ratio)",
+                    "frac_of_nominal_dense": achieved / NOMINAL_FP8_DENSE_TFLOPS,
+                    "nominal_dense_peak": NOMINAL_FP8_DENSE_TFLOPS,
                     "traffic": recorded_traffic("grouped_ffn_mx", args.config),
                     "algorithmic_flop_per_launch": flop_layer}
     else:
