@@ -21,7 +21,11 @@ struct CombineSmem {
 
 // The whole CTA (nthreads threads) combines token t.  `cg` selects L2-coherent
 // loads for indices written earlier in the same launch by other CTAs.  With
-// `accumulate` the sum starts from the current out[t] instead of zero.
+// `accumulate` the sum starts from the current out[t] instead of zero.  RB > 1
+// issues the loads of RB rows before their fma steps (for launches with only a
+// token or two per CTA, where the rows' L2 round trips would otherwise run one
+// after another); the fma order per element, and so the result, is the same.
+template <int RB = 1>
 __device__ __forceinline__ void combine_token(const float4* __restrict__ y_perm, const int32_t* pair_row,
                                               const float* topk_w, int t, int H4, int k, float4* __restrict__ out,
                                               CombineSmem& sm, bool cg, bool accumulate = false) {
@@ -55,22 +59,30 @@ __device__ __forceinline__ void combine_token(const float4* __restrict__ y_perm,
             a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (accumulate && v0 + u * bd < H4) a[u] = o[v0 + u * bd];
         }
-        for (int q = 0; q < nr; ++q) {
-            const float4* row = y_perm + (size_t)sm.rows[q] * H4;
-            const float w = sm.wts[q];
-            float4 y[U];
+        for (int q0 = 0; q0 < nr; q0 += RB) {
+            float4 y[RB][U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * bd;
-                y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (v < H4) y[u] = cg ? __ldcg(row + v) : __ldg(row + v);
+            for (int qq = 0; qq < RB; ++qq) {
+                const bool live = q0 + qq < nr;
+                const float4* row = y_perm + (size_t)sm.rows[live ? q0 + qq : 0] * H4;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int v = v0 + u * bd;
+                    y[qq][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (live && v < H4) y[qq][u] = cg ? __ldcg(row + v) : __ldg(row + v);
+                }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                a[u].x = fmaf(w, y[u].x, a[u].x);
-                a[u].y = fmaf(w, y[u].y, a[u].y);
-                a[u].z = fmaf(w, y[u].z, a[u].z);
-                a[u].w = fmaf(w, y[u].w, a[u].w);
+            for (int qq = 0; qq < RB; ++qq) {
+                if (q0 + qq >= nr) break;
+                const float w = sm.wts[q0 + qq];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    a[u].x = fmaf(w, y[qq][u].x, a[u].x);
+                    a[u].y = fmaf(w, y[qq][u].y, a[u].y);
+                    a[u].z = fmaf(w, y[qq][u].z, a[u].z);
+                    a[u].w = fmaf(w, y[qq][u].w, a[u].w);
+                }
             }
         }
 #pragma unroll

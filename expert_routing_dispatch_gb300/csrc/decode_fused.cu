@@ -38,6 +38,7 @@ using namespace gemm;
 
 constexpr long long GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles
 constexpr int SMALL_ROWS = 32;                    // token rows of the m-tiles and their boxes
+constexpr int FUSED_MAX_CTA_PAIRS = 256;          // pairs of one CTA's token slice (ceil(T / grid) * k)
 static_assert(SMALL_ROWS == AR, "token boxes are the GEMM core's m-tiles");
 
 struct FusedArgs {
@@ -64,6 +65,7 @@ struct FusedArgs {
 struct FusedSmem {
     int hist_before[MAX_LOCAL];  // local pairs of each expert before this CTA's slice
     int cursor[MAX_LOCAL];       // next grouped row of each expert for this CTA
+    int prow[FUSED_MAX_CTA_PAIRS];  // grouped row (or -1) of each pair of this CTA's tokens
     int rows[32];
     CombineSmem comb;
     int ok;
@@ -162,11 +164,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fs.hist_before[e] = 0;
         }
         __syncthreads();
-        for (long long q = threadIdx.x; q < P; q += NUM_THREADS) {
-            const int e = __ldcg(a.topk_idx + q) - a.e0;
-            if (e >= 0 && e < n) {
-                atomicAdd(&hist_all[e], 1);
-                if (q < p0) atomicAdd(&fs.hist_before[e], 1);
+        for (long long q0 = threadIdx.x; q0 < P; q0 += 8ll * NUM_THREADS) {
+            int ev[8];  // eight independent loads in flight, then the counts
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const long long q = q0 + (long long)u * NUM_THREADS;
+                ev[u] = q < P ? __ldcg(a.topk_idx + q) - a.e0 : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const long long q = q0 + (long long)u * NUM_THREADS;
+                const int e = ev[u];
+                if (e >= 0 && e < n) {
+                    atomicAdd(&hist_all[e], 1);
+                    if (q < p0) atomicAdd(&fs.hist_before[e], 1);
+                }
             }
         }
         __syncthreads();
@@ -211,29 +223,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if ((peers & lt) == 0) fs.cursor[e] = base + __popc(peers);
                     a.row_pair[row] = (int32_t)q;
                     a.pair_row[q] = row;
+                    fs.prow[q - p0] = row;
                 } else if (valid) {
                     a.pair_row[q] = -1;
+                    fs.prow[q - p0] = -1;
                 }
                 __syncwarp();
             }
         }
         __syncthreads();
+        // copy the x rows of this CTA's tokens to their local rows: one item per (token,
+        // 16-byte vector), four loads in flight per thread, then their stores
         const int H8 = a.H / 8;
-        for (int t = t0; t < t1 && !a.gather; ++t) {  // copy x rows of this CTA's tokens
-            if (threadIdx.x < 32) {
-                const int r = (lane < k) ? a.pair_row[(size_t)t * k + lane] : -1;
-                const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
-                if (r >= 0) fs.rows[__popc(m & ((1u << lane) - 1u))] = r;
-                if (lane == 0) fs.comb.nrows = __popc(m);
+        const int items = a.gather ? 0 : (t1 - t0) * H8;
+        for (int i0 = threadIdx.x; i0 < items; i0 += 4 * NUM_THREADS) {
+            uint4 val[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * NUM_THREADS;
+                if (i < items) val[u] = __ldg(a.x + (size_t)t0 * H8 + i);
             }
-            __syncthreads();
-            const int nr = fs.comb.nrows;
-            for (int v = threadIdx.x; v < H8; v += NUM_THREADS) {
-                const uint4 val = __ldg(a.x + (size_t)t * H8 + v);
-                for (int i = 0; i < nr; ++i) a.x_perm[(size_t)fs.rows[i] * H8 + v] = val;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * NUM_THREADS;
+                if (i >= items) break;
+                const int tl = i / H8, v = i - tl * H8;
+                for (int j = 0; j < k; ++j) {
+                    const int r = fs.prow[tl * k + j];
+                    if (r >= 0) a.x_perm[(size_t)r * H8 + v] = val[u];
+                }
             }
-            __syncthreads();
         }
+        __syncthreads();
         asm volatile("fence.proxy.async.global;" ::: "memory");  // x_perm is read by TMA next
         ok = grid_sync(a, 2u * G + (unsigned)a.stall, fs);
     }
@@ -264,8 +285,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) {
         const int H4 = a.H / 4;
         for (int t = blockIdx.x; t < T; t += G)
-            combine_token(reinterpret_cast<const float4*>(a.y_perm), a.pair_row, a.topk_w, t, H4, k,
-                          reinterpret_cast<float4*>(a.out), fs.comb, true);
+            combine_token<8>(reinterpret_cast<const float4*>(a.y_perm), a.pair_row, a.topk_w, t, H4, k,
+                             reinterpret_cast<float4*>(a.out), fs.comb, true);
     }
 
     __syncthreads();
@@ -285,6 +306,7 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
     if (attr != cudaSuccess) return attr;
     const int n = e1 - e0;
     const long long rows = (long long)T * k;
+    if ((long long)((T + sm_count() - 1) / sm_count()) * k > FUSED_MAX_CTA_PAIRS) return cudaErrorInvalidConfiguration;
     // 256-row weight tiles.  (128-row tiles for few local experts measured slower:
     // each tile then reloads its token tile for half the work.)
     const int grid = sm_count();

@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
 //   and P3.  sync[0] (arrivals) and sync[1] (abort) are zero at launch.
 constexpr long long MX_GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
 constexpr int MX_SMALL_ROWS = 32;                     // token rows of the fused launch's m-tiles and boxes
+constexpr int MX_FUSED_MAX_CTA_PAIRS = 256;           // pairs of one CTA's token slice (ceil(T / grid) * k)
 
 struct MxFusedArgs {
     const float* logits;
@@ -133,6 +134,7 @@ struct MxFusedArgs {
 struct MxFusedSmem {
     int hist_before[mx::MAX_LOCAL];  // local pairs of each expert before this CTA's slice
     int cursor[mx::MAX_LOCAL];       // next grouped row of each expert for this CTA
+    int prow[MX_FUSED_MAX_CTA_PAIRS];  // grouped row (or -1) of each pair of this CTA's tokens
     int rows[32];
     CombineSmem comb;
     int ok;
@@ -225,11 +227,21 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
             fs.hist_before[e] = 0;
         }
         __syncthreads();
-        for (long long q = threadIdx.x; q < P; q += mx::NUM_THREADS) {
-            const int e = __ldcg(a.topk_idx + q) - a.e0;
-            if (e >= 0 && e < n) {
-                atomicAdd(&hist_all[e], 1);
-                if (q < p0) atomicAdd(&fs.hist_before[e], 1);
+        for (long long q0 = threadIdx.x; q0 < P; q0 += 8ll * mx::NUM_THREADS) {
+            int ev[8];  // eight independent loads in flight, then the counts
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const long long q = q0 + (long long)u * mx::NUM_THREADS;
+                ev[u] = q < P ? __ldcg(a.topk_idx + q) - a.e0 : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const long long q = q0 + (long long)u * mx::NUM_THREADS;
+                const int e = ev[u];
+                if (e >= 0 && e < n) {
+                    atomicAdd(&hist_all[e], 1);
+                    if (q < p0) atomicAdd(&fs.hist_before[e], 1);
+                }
             }
         }
         __syncthreads();
@@ -274,47 +286,44 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
                     if ((peers & lt) == 0) fs.cursor[e] = base + __popc(peers);
                     a.row_pair[row] = (int32_t)q;
                     a.pair_row[q] = row;
+                    fs.prow[q - p0] = row;
                 } else if (valid) {
                     a.pair_row[q] = -1;
+                    fs.prow[q - p0] = -1;
                 }
                 __syncwarp();
             }
         }
         __syncthreads();
+        // quantise each token row of this CTA's slice once and copy it to the token's
+        // local rows: one item per (token, 32-element block), all in flight together
         const int H8 = a.H / 8, nblk = a.H / 32;
-        for (int t = t0; t < t1; ++t) {  // quantise each token row once, copy to its local rows
-            if (threadIdx.x < 32) {
-                const int r = (lane < k) ? a.pair_row[(size_t)t * k + lane] : -1;
-                const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
-                if (r >= 0) fs.rows[__popc(m & ((1u << lane) - 1u))] = r;
-                if (lane == 0) fs.comb.nrows = __popc(m);
-            }
-            __syncthreads();
-            const int nr = fs.comb.nrows;
-            for (int b = threadIdx.x; nr > 0 && b < nblk; b += mx::NUM_THREADS) {
-                float v[32];
+        for (int i = threadIdx.x; i < (t1 - t0) * nblk; i += mx::NUM_THREADS) {
+            const int tl = i / nblk, b = i - tl * nblk;
+            const size_t t = (size_t)(t0 + tl);
+            float v[32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 u = __ldg(a.x + (size_t)t * H8 + b * 4 + i);
-                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+            for (int j = 0; j < 4; ++j) {
+                const uint4 u = __ldg(a.x + t * H8 + b * 4 + j);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        v[8 * i + 2 * j] = bf16_lo(w4[j]);
-                        v[8 * i + 2 * j + 1] = bf16_hi(w4[j]);
-                    }
-                }
-                uint32_t w[8];
-                const uint8_t code = (uint8_t)mx::mx_quantize32(v, w);
-                for (int i = 0; i < nr; ++i) {
-                    const size_t row = (size_t)fs.rows[i];
-                    uint4* dst = reinterpret_cast<uint4*>(a.xpq + row * a.H + 32 * b);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    a.xps[row * nblk + b] = code;
+                for (int jj = 0; jj < 4; ++jj) {
+                    v[8 * j + 2 * jj] = bf16_lo(w4[jj]);
+                    v[8 * j + 2 * jj + 1] = bf16_hi(w4[jj]);
                 }
             }
-            __syncthreads();
+            uint32_t w[8];
+            const uint8_t code = (uint8_t)mx::mx_quantize32(v, w);
+            for (int j = 0; j < k; ++j) {
+                const int r = fs.prow[tl * k + j];
+                if (r < 0) continue;
+                uint4* dst = reinterpret_cast<uint4*>(a.xpq + (size_t)r * a.H + 32 * b);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                a.xps[(size_t)r * nblk + b] = code;
+            }
         }
+        __syncthreads();
         asm volatile("fence.proxy.async.global;" ::: "memory");  // xpq is read by TMA next
         ok = mx_grid_sync(a, 2u * G, fs);
     }
@@ -373,8 +382,8 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
     if (ok) {
         const int H4 = a.H / 4;
         for (int t = blockIdx.x; t < T; t += G)
-            combine_token(reinterpret_cast<const float4*>(a.y_perm), a.pair_row, a.topk_w, t, H4, k,
-                          reinterpret_cast<float4*>(a.out), fs.comb, true);
+            combine_token<8>(reinterpret_cast<const float4*>(a.y_perm), a.pair_row, a.topk_w, t, H4, k,
+                             reinterpret_cast<float4*>(a.out), fs.comb, true);
     }
 
     __syncthreads();
@@ -438,6 +447,7 @@ cudaError_t launch_layer_mx_fused(const uint16_t* x, const float* logits, const 
     if (attr != cudaSuccess) return attr;
     const int n = e1 - e0;
     const long long rows = (long long)T * k;
+    if ((long long)((T + sm_count() - 1) / sm_count()) * k > MX_FUSED_MAX_CTA_PAIRS) return cudaErrorInvalidConfiguration;
     CUtensorMap mG, mU, mD, mXs, mHs;
     if (!make_tmap_u8(&mG, wgq, (long long)n * I, H, mx::BN / 2) ||
         !make_tmap_u8(&mU, wuq, (long long)n * I, H, mx::BN / 2) ||
