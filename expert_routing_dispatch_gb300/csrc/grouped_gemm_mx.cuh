@@ -295,6 +295,9 @@ __device__ __forceinline__ void run(Ctl<G::STAGES>& c, uint32_t ring, Pipe& pipe
         (void)w0;
         (void)t0;
         const uint64_t pol = l2_policy_evict_last();
+        // the fused decode's down phase streams its weights once while it writes y_perm,
+        // which the combine phase reads next: those weights go first out of L2
+        const uint64_t wpol = (AR == 32 && MODE == MODE_DOWN) ? l2_policy_evict_first() : pol;
         int g = pipe.g;
         bool ok = true;
         for (int tile = blockIdx.x; ok && !__any_sync(0xffffffffu, *abort_flag) && next_tile<G>(c, n, tile, e_hint, tc);
@@ -317,12 +320,12 @@ __device__ __forceinline__ void run(Ctl<G::STAGES>& c, uint32_t ring, Pipe& pipe
                     const uint32_t fb = smem_u32(&c.full[s]);
                     mbar_arrive_expect_tx(fb, stage_tx);
                     if (MODE == MODE_GATEUP) {  // [96 gate rows | 96 up rows]
-                        tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
-                        tma_load_2d(b_addr(s) + (uint32_t)(BN / 2) * BKB, tmB1, kb * BKB, b_row, fb, pol);
+                        tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, wpol);
+                        tma_load_2d(b_addr(s) + (uint32_t)(BN / 2) * BKB, tmB1, kb * BKB, b_row, fb, wpol);
                         tma_load_2d(a_addr(s), tma, kb * BKB, a_row, fb, pol);
                     } else {
                         tma_load_2d(a_addr(s), tma, kb * BKB, a_row, fb, pol);
-                        tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, pol);
+                        tma_load_2d(b_addr(s), tmB0, kb * BKB, b_row, fb, wpol);
                     }
                 }
                 __syncwarp();
