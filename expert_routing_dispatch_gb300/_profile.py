@@ -11,6 +11,13 @@
         untouched: the counters exist only in the copy built here
         (_lib/libmoe_prof.so).
 
+    python -m expert_routing_dispatch_gb300._profile phases [workload ...]
+        Where the fused single-launch layers (bf16 moe_layer and moe_layer_mxfp8 at
+        T*k <= MOE_FUSED_MAX_PAIRS) spend their time.  The same profile copy of the
+        library stamps %globaltimer in every CTA at each phase boundary (after a block
+        barrier); per phase the table gives the time from the last CTA entering it to
+        the last CTA leaving it (medians of 6 launches, L2 flushed before each).
+
     python -m expert_routing_dispatch_gb300._profile steps [--config W] [--warmup N] [--steps K] [--precision P]
         A short, fixed launch sequence of the product library for ncu: N + K
         moe_layer (or moe_layer_mxfp8) steps with a 256 MiB L2 flush before each,
@@ -162,6 +169,72 @@ def steps(argv):
     print(f"steps ok: {a.config} {a.precision}: {a.warmup + a.steps} layer steps, then the split entries once")
 
 
+PHASES = ("route", "barrier", "dispatch", "barrier", "gate/up GEMM", "barrier", "down GEMM", "barrier", "combine",
+          "teardown")
+
+
+def phases(argv):
+    import statistics
+
+    import numpy as np
+    import torch
+
+    import expert_routing_dispatch_gb300 as moe
+    import synth
+    from expert_routing_dispatch_gb300 import _build
+
+    _build.build(force=True, extra_flags=["-DMOE_GEMM_PROFILE"], out_lib=PROF_LIB)
+    moe.LIB_PATH = PROF_LIB
+    L = moe.lib()
+    L.moe_debug_phase_mx.argtypes = [ctypes.c_void_p]
+    L.moe_debug_phase_bf.argtypes = [ctypes.c_void_p]
+    dev = torch.device("cuda")
+    print("| workload | precision | launch us | " + " | ".join(PHASES) + " |")
+    print("|---|---|---" + "|---" * len(PHASES) + "|")
+    for name in argv or ["decode", "one_token_per_expert_ep1", "one_token_per_expert_ep4"]:
+        cfg = synth.config(name)
+        T, H, I, E, k, e0, e1 = synth.dims_of(cfg)
+        n = e1 - e0
+        assert T * k <= moe.FUSED_MAX_PAIRS, name
+        inp = synth.make_inputs(cfg)
+        g = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+        x, lg, wg, wu, wd = (g(inp[nm]) for nm in ("x", "logits", "w_gate", "w_up", "w_down"))
+        wq = {}
+        for key, w_, r_, K_ in (("g", wg, n * I, H), ("u", wu, n * I, H), ("d", wd, n * H, I)):
+            q_ = torch.empty((r_, K_), dtype=torch.uint8, device=dev)
+            s_ = torch.empty((r_, K_ // 32), dtype=torch.uint8, device=dev)
+            moe.moe_quantize_mxfp8(w_, r_, K_, q_, s_)
+            wq[key] = (q_, s_)
+        out = torch.empty((T, H), dtype=torch.float32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        wsb = moe.alloc_workspace(moe.moe_workspace_size(cfg))
+        wsm = moe.alloc_workspace(moe.moe_layer_mxfp8_workspace_size(cfg))
+        runs = (("bf16", lambda: moe.moe_layer(cfg, x, lg, wg, wu, wd, out, wsb, status=status), L.moe_debug_phase_bf),
+                ("mxfp8", lambda: moe.moe_layer_mxfp8(cfg, x, lg, wq["g"], wq["u"], wq["d"], out, wsm, status=status),
+                 L.moe_debug_phase_mx))
+        for prec, launch, read in runs:
+            per = [[] for _ in PHASES]
+            total = []
+            for rep_ in range(8):
+                flush.zero_()
+                torch.cuda.synchronize()
+                launch()
+                torch.cuda.synchronize()
+                assert int(status.item()) == 0
+                buf = (ctypes.c_ulonglong * (1024 * 12))()
+                assert read(buf) == 0
+                ts = np.frombuffer(buf, dtype=np.uint64).reshape(1024, 12)[:torch.cuda.get_device_properties(0)
+                                                                          .multi_processor_count, :11].astype(np.int64)
+                if rep_ < 2:
+                    continue
+                for i in range(len(PHASES)):
+                    per[i].append((ts[:, i + 1].max() - ts[:, i].max()) / 1e3)
+                total.append((ts[:, 10].max() - ts[:, 0].min()) / 1e3)
+            print(f"| {name} | {prec} | {statistics.median(total):.1f} | " +
+                  " | ".join(f"{statistics.median(v):.1f}" for v in per) + " |", flush=True)
+
+
 def roles(argv):
     import torch
 
@@ -183,4 +256,4 @@ def roles(argv):
 if __name__ == "__main__":
     sys.path.insert(0, ROOT)
     cmd, rest = (sys.argv[1], sys.argv[2:]) if len(sys.argv) > 1 else ("roles", [])
-    {"roles": roles, "steps": steps}[cmd](rest)
+    {"roles": roles, "steps": steps, "phases": phases}[cmd](rest)

@@ -36,6 +36,23 @@ namespace {
 
 using namespace gemm;
 
+#ifdef MOE_GEMM_PROFILE
+// Tuning builds only: %globaltimer (ns) of every CTA at the phase boundaries of the
+// fused launch (after a block barrier), read back by moe_debug_phase_bf.
+__device__ unsigned long long g_phase_bf[1024][12];
+#define PHASE_STAMP(i)                                                              \
+    do {                                                                            \
+        __syncthreads();                                                            \
+        if (threadIdx.x == 0 && blockIdx.x < 1024) {                                \
+            unsigned long long t_;                                                  \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));              \
+            g_phase_bf[blockIdx.x][i] = t_;                                          \
+        }                                                                           \
+    } while (0)
+#else
+#define PHASE_STAMP(i) ((void)0)
+#endif
+
 constexpr long long GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles
 constexpr int SMALL_ROWS = 32;                    // token rows of the m-tiles and their boxes
 constexpr int FUSED_MAX_CTA_PAIRS = 256;          // pairs of one CTA's token slice (ceil(T / grid) * k)
@@ -143,6 +160,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     Pipe p;
     pipe_reset(p);
+    PHASE_STAMP(0);
 
     // ---------------- P0: route
     {
@@ -150,7 +168,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = blockIdx.x * warps + warp; t < T; t += G * warps)
             route_token_any(a.logits, t, a.E, k, a.topk_idx, a.topk_w, a.status);
     }
+    PHASE_STAMP(1);
     bool ok = grid_sync(a, 1u * G + (unsigned)a.stall, fs);
+    PHASE_STAMP(2);
 
     // ---------------- P1: dispatch
     if (ok) {
@@ -256,7 +276,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncthreads();
         asm volatile("fence.proxy.async.global;" ::: "memory");  // x_perm is read by TMA next
+        PHASE_STAMP(3);
         ok = grid_sync(a, 2u * G + (unsigned)a.stall, fs);
+        PHASE_STAMP(4);
     }
 
     // ---------------- P2: gate/up GEMM + SiLU*up
@@ -268,7 +290,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             run_phase<MODE_GATEUP>(c, ring, p, &tmXg, &wmGU, ga, a.row_pair, k);
         else
             run_phase<MODE_GATEUP>(c, ring, p, &tmXs, &wmGU, ga);
+        PHASE_STAMP(5);
         ok = grid_sync(a, 3u * G + (unsigned)a.stall, fs) && !c.abort_flag;
+        PHASE_STAMP(6);
     }
 
     // ---------------- P3: down GEMM
@@ -278,7 +302,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         build_tile_table(c, n, da.ntiles_n, da.bn);
         __syncthreads();
         run_phase<MODE_DOWN>(c, ring, p, &tmHs, &wmD, da);
+        PHASE_STAMP(7);
         ok = grid_sync(a, 4u * G + (unsigned)a.stall, fs) && !c.abort_flag;
+        PHASE_STAMP(8);
     }
 
     // ---------------- P4: combine
@@ -290,7 +316,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     __syncthreads();
+    PHASE_STAMP(9);
     teardown(c, p, a.status);
+    PHASE_STAMP(10);
 }
 
 }  // namespace
@@ -337,3 +365,10 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
 }
 
 }  // namespace moe
+
+#ifdef MOE_GEMM_PROFILE
+// tuning builds only: the phase timestamps of the fused launch ([1024][12] ns)
+extern "C" int moe_debug_phase_bf(unsigned long long* host) {
+    return cudaMemcpyFromSymbol(host, moe::g_phase_bf, sizeof(moe::g_phase_bf)) == cudaSuccess ? 0 : 4;
+}
+#endif

@@ -104,6 +104,23 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
 //   scales to every local row); P2 MX gate/up; P3 MX down; P4 combine.  The MX GEMM
 //   core (grouped_gemm_mx.cuh) keeps its ring and accumulator counters across P2
 //   and P3.  sync[0] (arrivals) and sync[1] (abort) are zero at launch.
+#ifdef MOE_GEMM_PROFILE
+// Tuning builds only: %globaltimer (ns) of every CTA at the phase boundaries of the
+// fused launch (after a block barrier), read back by moe_debug_phase_mx.
+__device__ unsigned long long g_phase_mx[1024][12];
+#define PHASE_STAMP(i)                                                              \
+    do {                                                                            \
+        __syncthreads();                                                            \
+        if (threadIdx.x == 0 && blockIdx.x < 1024) {                                \
+            unsigned long long t_;                                                  \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));              \
+            g_phase_mx[blockIdx.x][i] = t_;                                          \
+        }                                                                           \
+    } while (0)
+#else
+#define PHASE_STAMP(i) ((void)0)
+#endif
+
 constexpr long long MX_GRID_WAIT_LIMIT = 1ll << 31;  // clock cycles (~1 s)
 constexpr int MX_SMALL_ROWS = 32;                     // token rows of the fused launch's m-tiles and boxes
 constexpr int MX_FUSED_MAX_CTA_PAIRS = 256;           // pairs of one CTA's token slice (ceil(T / grid) * k)
@@ -206,6 +223,7 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     mx::Pipe pipe{0, 0};
+    PHASE_STAMP(0);
 
     // ---------------- P0: route
     {
@@ -213,7 +231,9 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
         for (int t = blockIdx.x * warps + warp; t < T; t += G * warps)
             route_token_any(a.logits, t, a.E, k, a.topk_idx, a.topk_w, a.status);
     }
+    PHASE_STAMP(1);
     bool ok = mx_grid_sync(a, 1u * G, fs);
+    PHASE_STAMP(2);
 
     // ---------------- P1: dispatch, x quantised to MXFP8 once per token
     if (ok) {
@@ -325,7 +345,9 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
         }
         __syncthreads();
         asm volatile("fence.proxy.async.global;" ::: "memory");  // xpq is read by TMA next
+        PHASE_STAMP(3);
         ok = mx_grid_sync(a, 2u * G, fs);
+        PHASE_STAMP(4);
     }
 
     // ---------------- P2: MX gate/up GEMM + SiLU*up, h quantised to MXFP8
@@ -350,7 +372,9 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
         __syncthreads();
         mx::run<mx::MODE_GATEUP, GD>(c, ring, pipe, &tmXs, &tmG, &tmU, ga);
         mx::pipe_advance(c, pipe, n, ga.kblocks);
+        PHASE_STAMP(5);
         ok = mx_grid_sync(a, 3u * G, fs) && !c.abort_flag;
+        PHASE_STAMP(6);
     }
 
     // ---------------- P3: MX down GEMM
@@ -375,7 +399,9 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
         __syncthreads();
         mx::run<mx::MODE_DOWN, GD>(c, ring, pipe, &tmHs, &tmD, &tmD, da);
         mx::pipe_advance(c, pipe, n, da.kblocks);
+        PHASE_STAMP(7);
         ok = mx_grid_sync(a, 4u * G, fs) && !c.abort_flag;
+        PHASE_STAMP(8);
     }
 
     // ---------------- P4: combine
@@ -387,7 +413,9 @@ __global__ void __launch_bounds__(mx::NUM_THREADS, 1)
     }
 
     __syncthreads();
+    PHASE_STAMP(9);
     mx::teardown(c, a.status);
+    PHASE_STAMP(10);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -542,6 +570,9 @@ cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int
 
 #ifdef MOE_GEMM_PROFILE
 // tuning builds only: read (and optionally reset) the role counters of grouped_gemm_mx.cuh
+extern "C" int moe_debug_phase_mx(unsigned long long* host) {
+    return cudaMemcpyFromSymbol(host, moe::g_phase_mx, sizeof(moe::g_phase_mx)) == cudaSuccess ? 0 : 4;
+}
 extern "C" int moe_debug_mx_prof(unsigned long long* host24, int reset) {
     cudaError_t e = cudaMemcpyFromSymbol(host24, moe::mx::g_mx_prof, sizeof(unsigned long long) * 24);
     if (reset) {
