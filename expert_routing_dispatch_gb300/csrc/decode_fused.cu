@@ -297,8 +297,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // ---------------- P3: down GEMM
     if (ok) {
-        // K = 2 I: h as hi and lo terms, each pair of k-blocks against one weight k-block
-        const Args da{a.y_perm, a.status, n, 2 * a.I / BK, (a.H + a.bn - 1) / a.bn, a.H, a.H, a.bn, a.bn, 1, 0};
+        // h as hi and lo terms: every stage holds a W_down k-block with the hi and the lo
+        // k-block of h that use it (K = I weight k-blocks, 2 I columns of h)
+        const Args da{a.y_perm, a.status, n, a.I / BK, (a.H + a.bn - 1) / a.bn, a.H, a.H, a.bn, a.bn, 1, 0};
         build_tile_table(c, n, da.ntiles_n, da.bn);
         __syncthreads();
         run_phase<MODE_DOWN>(c, ring, p, &tmHs, &wmD, da);

@@ -10,24 +10,26 @@
 //   gate/up : acc[128 x 256] = x_perm[rows] . [W_gate[e] rows n..n+127 ; W_up[e] rows n..n+127]^T
 //             epilogue h = silu(acc[:, 0:128]) * acc[:, 128:256] (fp32 math), stored
 //             as two bf16 terms hi + lo in the split layout [rows, 2 I] (common.cuh)
-//   down    : acc[128 x 256] = h[rows] . W_down[e][n..n+255]^T over K = 2 I: the
-//             k-blocks alternate hi and lo of h against the same weight k-block,
-//             so y_perm = W_down (hi + lo) (fp32)
+//   down    : acc[128 x 256] = h[rows] . W_down[e][n..n+255]^T over K = I weight
+//             k-blocks: each stage holds a W_down k-block with the hi and the lo
+//             k-block of h that use it, so y_perm = W_down (hi + lo) (fp32)
 // Tiles are (expert, m-tile of 32 rows, n-tile); the tile table is built on
 // the device from the row offsets.  Decode has ~16 rows per expert, so a stage
-// carries 32 token rows (4 KB) next to its 256 weight rows; the MMA keeps M = 128,
-// its A rows 32..127 read the bytes after the token slot (inside the ring) and
-// only feed accumulator rows that are never stored.  Within an expert the m-tiles of one n-tile
-// are consecutive, so CTAs running side by side share a weight tile through L2.
+// carries 32-row token k-blocks (4 KB each: gate/up uses one, down its hi and lo)
+// next to a 32 KB weight k-block; the MMA keeps M = 128, its A rows 32..127 read
+// the bytes after the token slot (inside the ring) and only feed accumulator rows
+// that are never stored.  Within an expert the m-tiles of one n-tile are
+// consecutive, so CTAs running side by side share a weight tile through L2.
 // When the last round of tiles would leave most CTAs idle (r tiles, 2r or 4r <=
 // CTAs), each of those r tiles is split along N into 2 or 4 pieces (narrower
 // MMA N, weight boxes and epilogue), which spreads the last round over more SMs.
 //
 // CTA = 6 warps: warp 0 issues TMA loads (128-byte swizzle) into a 5-stage
-// shared-memory ring (160 KB of weights in flight); warp 1 owns 512 TMEM columns (two 256-column fp32
-// accumulators) and issues tcgen05.mma (M=128, N=256, K=16) from one elected
-// lane while all 32 lanes run the loop; warps 2..5 drain TMEM with tcgen05.ld
-// and run the epilogue while the next tile accumulates into the other buffer.
+// shared-memory ring of 40 KB stages (160 KB of weights in flight, in both phases);
+// warp 1 owns 512 TMEM columns (two 256-column fp32 accumulators) and issues
+// tcgen05.mma (M=128, N=256, K=16) from one elected lane while all 32 lanes run
+// the loop; warps 2..5 drain TMEM with tcgen05.ld and run the epilogue while the
+// next tile accumulates into the other buffer.
 // Every wait is bounded: on timeout the status word gets MOE_ERR_TIMEOUT and
 // all roles bail out.
 #pragma once
@@ -42,9 +44,10 @@ namespace gemm {
 constexpr int BM = 128, BN = 256, BK = 64, AR = 32, STAGES = 5;
 static_assert(AR <= 32 && AR % 4 == 0, "one producer lane per m-tile row; four-row gathers");
 constexpr int ROW_BYTES = BK * 2;     // bytes of one K-row of a tile = swizzle span
-constexpr int A_BYTES = AR * BK * 2;  // 4 KB
+constexpr int A_BYTES = AR * BK * 2;  // 4 KB per token k-block
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+// a stage: [token k-block (gate/up; hi of h for down) | lo of h (down) | weight k-block]
+constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_LOCAL = 1024;
@@ -68,7 +71,7 @@ __device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const void* tmap, i
 struct Ctl {
     // per epilogue warp: a 32-row x 128-byte staging tile (16-byte slots XOR-swizzled by
     // row) that turns per-row TMEM reads into whole 128-byte row segments in global memory
-    alignas(128) uint4 stage[4][32 * 8];
+    alignas(128) uint4 stage[AR / 32][32 * 8];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t tfull[2];
@@ -94,7 +97,7 @@ struct Args {
     int b_rows;       // weight rows per expert in the B tensor map (I or H)
     int n_step;       // output columns per n-tile (bn / 2 for gate/up, bn for down)
     int bn;           // MMA N = weight rows per tile (256; 128 also supported)
-    int ksplit;       // weight k-block of token k-block kb: kb >> ksplit (1 for down: hi and lo share it)
+    int hilo;         // 1 (down): a stage carries the hi and the lo token k-block of its weight k-block
     int stall;        // testing hook: extra arrivals ring stage 0 waits for (0 in normal use)
 };
 
@@ -225,7 +228,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
     const int n = args.n;
     volatile int* abort_flag = &c.abort_flag;
     auto a_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES); };
-    auto b_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES + A_BYTES); };
+    auto b_addr = [&](int s) { return ring + (uint32_t)(s * STAGE_BYTES + 2 * A_BYTES); };
 
     if (warp == 0) {
         // ================= TMA producer: the whole warp loops, the elected lane issues =================
@@ -242,7 +245,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             const CUtensorMap* tmB0 = &wm->b0[tc.shift];
             const CUtensorMap* tmB1 = &wm->b1[tc.shift];
             const CUtensorMap* tma_a = tmA;
-            const uint32_t stage_tx = (uint32_t)(AR * BK * 2 + bn_t * BK * 2);
+            const uint32_t stage_tx = (uint32_t)((1 + args.hilo) * AR * BK * 2 + bn_t * BK * 2);
             int tok = 0;  // gather: lane i holds the token of m-tile row i (written earlier in the launch)
             if (gather_pairs != nullptr) {
                 const int valid = tc.cnt - tc.mt * AR;
@@ -261,12 +264,16 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                 if (leader) {
                     // Each copy takes ~100 cycles to issue.  Gate/up issues its two weight
                     // boxes before the token box; down keeps the token box first.
-                    const int wk = (kb >> args.ksplit) * BK;
+                    const int wk = kb * BK;
                     mbar_arrive_expect_tx(fb, stage_tx);
                     if (MODE == MODE_GATEUP) {  // [gate rows | up rows], bn_t/2 each
                         tma_load_2d(b_addr(s), tmB0, wk, b_row, fb, pol_b);
                         tma_load_2d(b_addr(s) + (uint32_t)(bn_t / 2) * BK * 2, tmB1, wk, b_row, fb, pol_b);
                         if (gather_pairs == nullptr) tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
+                    } else if (args.hilo) {  // h k-blocks 2 kb (hi) and 2 kb + 1 (lo) of the split layout
+                        tma_load_2d(a_addr(s), tma_a, 2 * kb * BK, a_row, fb, pol_a);
+                        tma_load_2d(a_addr(s) + (uint32_t)A_BYTES, tma_a, (2 * kb + 1) * BK, a_row, fb, pol_a);
+                        tma_load_2d(b_addr(s), tmB0, wk, b_row, fb, pol_b);
                     } else {
                         tma_load_2d(a_addr(s), tma_a, kb * BK, a_row, fb, pol_a);
                         tma_load_2d(b_addr(s), tmB0, wk, b_row, fb, pol_b);
@@ -315,9 +322,14 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
                     // descriptors are linear in the address (bits 0-13 hold address >> 4)
                     const uint64_t ad = a_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
                     const uint64_t bd = b_desc0 + (uint64_t)((s * STAGE_BYTES) >> 4);
+                    // hilo: the hi k-block's four MMAs, then the lo k-block's against the same
+                    // weight k-block (the order of the split path's down GEMM)
+                    for (int sub = 0; sub <= args.hilo; ++sub) {
+                        const uint64_t as = ad + (uint64_t)((sub * A_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
-                        tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                        for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
+                            tc_mma_bf16(d_tmem, as + 2 * kk, bd + 2 * kk, idesc, (kb | kk | sub) != 0);
+                    }
                     tc_commit(smem_u32(&c.empty[s]));
                 }
                 __syncwarp();
@@ -340,7 +352,7 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
             const uint32_t taddr = c.tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const int bn_t = args.bn >> tc.shift;
             const int col0 = tc.nt * args.n_step + tc.piece * (args.n_step >> tc.shift);
-            uint4* st = c.stage[q];
+            uint4* st = c.stage[q < AR / 32 ? q : 0];
             if (q * 32 >= AR) {
                 // accumulator rows past the m-tile: computed from stale A rows, not stored
             } else if (MODE == MODE_GATEUP) {
