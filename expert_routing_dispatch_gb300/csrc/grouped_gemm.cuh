@@ -233,7 +233,10 @@ __device__ __forceinline__ void run_phase(Ctl& c, uint32_t ring, Pipe& p, const 
     if (warp == 0) {
         // ================= TMA producer: the whole warp loops, the elected lane issues =================
         const uint64_t pol_a = l2_policy_evict_last();  // token rows are reread for every n-tile
-        const uint64_t pol_b = l2_policy_evict_last();  // a weight tile is read by every m-tile of its expert
+        // a weight tile is read by every m-tile of its expert; the down phase streams its
+        // weights while it writes y_perm, which the combine phase reads next, so those
+        // weights go first out of L2
+        const uint64_t pol_b = MODE == MODE_DOWN ? l2_policy_evict_first() : l2_policy_evict_last();
         int e_hint = 0;
         TileCoord tc;
         bool ok = !__any_sync(0xffffffffu, *abort_flag);
