@@ -7,7 +7,9 @@
         waits), groups a workload's rows with moe_route + moe_dispatch, runs each
         GEMM three times as warm-up and then once more with L2 flushed between the
         counter reset and the read, and prints one markdown table row per GEMM:
-        wait cycles / the role's cycles in the kernel.  The product library is
+        wait cycles / the role's cycles in the kernel.  For decode-sized workloads
+        (T*k <= MOE_FUSED_MAX_PAIRS) the MXFP8 rows are the GEMM phases inside the
+        fused moe_layer_mxfp8 launch.  The product library is
         untouched: the counters exist only in the copy built here
         (_lib/libmoe_prof.so).
 
@@ -90,7 +92,7 @@ def measure(name):
         ms, c = timed(launch, L.moe_debug_gemm_prof, 16)
         c = c[:8] if mode == "gate/up" else c[8:]
         rows.append((f"bf16 {mode}", name, ms, c[7], _frac(c[3], c[4]), _frac(c[2], c[4]), _frac(c[0], c[1]),
-                     _frac(c[5], c[6])))
+                     _frac(c[5], c[6]), None))
     # MXFP8 FFN: [0..11] gate/up, [12..23] down (both GEMMs run in each launch)
     u8 = torch.uint8
     wq = {}
@@ -101,12 +103,20 @@ def measure(name):
     xq, xs = torch.empty((P, H), dtype=u8, device=dev), torch.empty((P, H // 32), dtype=u8, device=dev)
     moe.moe_quantize_mxfp8(x_perm, P, H, xq, xs)
     fws = moe.alloc_workspace(moe.moe_expert_ffn_mxfp8_workspace_size(cfg))
-    ms, c = timed(lambda: moe.moe_expert_ffn_mxfp8(cfg, xq, xs, offsets, wq["g"], wq["u"], wq["d"], y, fws,
-                                                    status=status), L.moe_debug_mx_prof, 24)
+    if P <= moe.FUSED_MAX_PAIRS:
+        # decode sizes: the GEMM phases inside the fused moe_layer_mxfp8 launch
+        lws = moe.alloc_workspace(moe.moe_layer_mxfp8_workspace_size(cfg))
+        out = torch.empty((T, H), dtype=torch.float32, device=dev)
+        launch, label = (lambda: moe.moe_layer_mxfp8(cfg, x, lg, wq["g"], wq["u"], wq["d"], out, lws,
+                                                     status=status)), "mxfp8 fused"
+    else:
+        launch, label = (lambda: moe.moe_expert_ffn_mxfp8(cfg, xq, xs, offsets, wq["g"], wq["u"], wq["d"], y, fws,
+                                                          status=status)), "mxfp8"
+    ms, c = timed(launch, L.moe_debug_mx_prof, 24)
     for j, mode in enumerate(("gate/up", "down")):
         cc = c[12 * j:12 * j + 12]
-        rows.append((f"mxfp8 {mode}", name, ms, cc[10], _frac(cc[3], cc[5]), _frac(cc[2], cc[5]), _frac(cc[0], cc[1]),
-                     _frac(cc[6], cc[7])))
+        rows.append((f"{label} {mode}", name, ms, cc[10], _frac(cc[3], cc[5]), _frac(cc[2], cc[5]),
+                     _frac(cc[0], cc[1]), _frac(cc[6], cc[7]), _frac(cc[8], cc[9])))
     return rows
 
 
@@ -246,11 +256,12 @@ def roles(argv):
     assert torch.cuda.is_available()
     names = argv or ["prefill_ep_rank", "prefill_full"]
     print("| GEMM | workload | launch ms (profile build) | tiles | MMA waits for data | MMA waits for epilogue "
-          "| producer waits | epilogue waits |")
-    print("|---|---|---|---|---|---|---|---|")
+          "| producer waits | epilogue waits | scale warps wait |")
+    print("|---|---|---|---|---|---|---|---|---|")
     for nm in names:
         for r in measure(nm):
-            print(f"| {r[0]} | {r[1]} | {r[2]:.4f} | {r[3]} | {r[4]:.2f} | {r[5]:.2f} | {r[6]:.2f} | {r[7]:.2f} |")
+            sw = "—" if r[8] is None else f"{r[8]:.2f}"
+            print(f"| {r[0]} | {r[1]} | {r[2]:.4f} | {r[3]} | {r[4]:.2f} | {r[5]:.2f} | {r[6]:.2f} | {r[7]:.2f} | {sw} |")
 
 
 if __name__ == "__main__":
