@@ -137,3 +137,33 @@ def test_layer_split_path_equals_split_entries(moe, name):
     b, ib, wb = split(moe, dims, inp)
     assert np.array_equal(ia, ib) and np.array_equal(wa.view(np.uint32), wb.view(np.uint32))
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("T", [256, 257])
+def test_fused_top32_at_threshold(moe, T):
+    # k = 32 (the largest slot count): T*k = 8192 runs fused (every CTA's slice holds up to
+    # 64 pairs), 8224 runs split; both equal the split entries and the oracle
+    H, I, E, k, e0, e1 = 128, 128, 40, 32, 4, 36
+    inp = small(T, H, I, E, k, e0, e1, seed=9)
+    dims = moe.Dims(T, H, I, E, k, e0, e1)
+    assert (T * k <= moe.FUSED_MAX_PAIRS) == (T == 256)
+    out, idx, w = layer(moe, dims, inp)
+    ref_split, ridx_s, rw_s = split(moe, dims, inp)
+    assert np.array_equal(idx, ridx_s) and np.array_equal(out.view(np.uint32), ref_split.view(np.uint32))
+    st, ridx, rw = oracle.route(inp["logits"], k)
+    assert np.array_equal(idx, ridx)
+    toks = sample_tokens(T, 64)
+    st, ref = oracle.moe_layer_tokens(inp["logits"], inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], k, e0, e1,
+                                      tokens=toks)
+    bound = bf16_h_bound(inp, k, e0, e1, toks, ridx, rw) + 1e-6 * np.abs(ref).max()
+    assert np.all(np.abs(out[toks].astype(np.float64) - ref) <= bound)
+    if T * k <= moe.FUSED_MAX_PAIRS:  # dispatch by TMA row gather on the same shape
+        import torch
+
+        o2 = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+        stt = torch.zeros(1, dtype=torch.int32, device="cuda")
+        moe.moe_layer_gather(dims, dev(inp["x"]), dev(inp["logits"]), dev(inp["w_gate"]), dev(inp["w_up"]),
+                             dev(inp["w_down"]), o2, moe.alloc_workspace(moe.moe_workspace_size(dims)), status=stt)
+        torch.cuda.synchronize()
+        assert int(stt.item()) == 0
+        assert np.array_equal(host(o2).view(np.uint32), out.view(np.uint32))

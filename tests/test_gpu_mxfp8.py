@@ -222,6 +222,7 @@ def test_mx_layer(moe, name):
     (300, 384, 640, 8, 2, 1, 5),      # I = 6.67 gate/up tiles of 96 columns, H = 2 down tiles of 192
     (513, 256, 128, 3, 1, 1, 2),      # one local expert, m-tile tail, I smaller than a gate/up tile
     (37, 128, 256, 8, 8, 2, 5),       # k = E, partial range
+    (256, 128, 128, 40, 32, 4, 36),   # k = 32 at T*k = 8192: the fused launch, 64 pairs per CTA slice
 ])
 def test_mx_layer_small_shapes(moe, dims):
     import torch
