@@ -402,8 +402,8 @@ def run_ours(args):
     # the timed step: one moe_layer call (decode-sized: one persistent launch; else
     # route + dispatch place/gather + gate/up + down + combine)
     names = ["layer_fused" if fused else "layer_mxfp8" if mx else "layer"]
-    # route, place, gather, gate/up, down, combine (+ the quantisation of x for MXFP8)
-    launches_per_step = 1 if fused or mx_fused else 7 if mx else 6
+    # route, place, row copy (for MXFP8: quantised once per token), gate/up, down, combine
+    launches_per_step = 1 if fused or mx_fused else 6
 
     def step(evs):
         evs[0].record(stream)

@@ -163,7 +163,7 @@ struct MxLayerWs {
     int32_t* row_pair;
     int32_t* pair_row;
     void* dispatch_ws;
-    uint8_t *xq, *xs, *xpq, *xps;
+    uint8_t *xpq, *xps;
     void* ffn_ws;
     float* y_perm;
     unsigned* sync;  // grid-barrier words of the fused launch
@@ -172,7 +172,7 @@ struct MxLayerWs {
 
 MxLayerWs carve_mx(const moe_dims* d, void* base) {
     MxLayerWs w{};
-    const size_t P = pairs_of(d), n = (size_t)(d->e1 - d->e0), T = (size_t)d->T, H = (size_t)d->H;
+    const size_t P = pairs_of(d), n = (size_t)(d->e1 - d->e0), H = (size_t)d->H;
     uint8_t* p = static_cast<uint8_t*>(base);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -188,8 +188,6 @@ MxLayerWs carve_mx(const moe_dims* d, void* base) {
     w.pair_row = reinterpret_cast<int32_t*>(take(P * 4));
     w.dispatch_bytes = align_up(dispatch_scratch_bytes((long long)d->T, (int)n));
     w.dispatch_ws = take(w.dispatch_bytes);
-    w.xq = take(T * H);
-    w.xs = take(T * H / 32);
     w.xpq = take(P * H);
     w.xps = take(P * H / 32);
     w.ffn_ws = take(mx_ffn_scratch_bytes((long long)P, d->I));
@@ -492,10 +490,9 @@ int moe_layer_mxfp8(const moe_dims* d, const uint16_t* x, const float* logits, c
     if (cudaMemsetAsync(hist, 0, w.dispatch_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_route_hist(logits, d->T, d->E, d->k, idx, wt, status_dev, hist, dispatch_chunk_tokens(d->T), d->e0, n,
                           s) != cudaSuccess ||
-        launch_mx_quantize(x, d->T, d->H, w.xq, w.xs, s) != cudaSuccess ||
         launch_dispatch_place(x, idx, hist, d->T, d->H, d->k, d->e0, d->e1, w.counts, w.offsets, w.row_pair,
                               w.pair_row, nullptr, s) != cudaSuccess ||
-        launch_mx_gather(w.xq, w.xs, d->T, d->H, d->k, w.pair_row, w.xpq, w.xps, s) != cudaSuccess ||
+        launch_mx_dispatch_quantize(x, d->T, d->H, d->k, w.pair_row, w.xpq, w.xps, s) != cudaSuccess ||
         launch_mx_expert_ffn(w.xpq, w.xps, w.offsets, w_gate_q, w_gate_s, w_up_q, w_up_s, w_down_q, w_down_s,
                              w.y_perm, (long long)pairs_of(d), d->H, d->I, n, w.ffn_ws, status_dev, s) != cudaSuccess ||
         launch_combine(w.y_perm, w.pair_row, wt, d->T, d->H, d->k, out, s) != cudaSuccess)

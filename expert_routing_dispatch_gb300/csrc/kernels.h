@@ -72,8 +72,9 @@ cudaError_t launch_layer_fused(const uint16_t* x, const float* logits, const uin
 
 // mxfp8.cu: the MXFP8 expert FFN (E4M3 codes, UE8M0 scales per 32 elements along K)
 cudaError_t launch_mx_quantize(const uint16_t* src, long long rows, int K, uint8_t* q, uint8_t* s, cudaStream_t st);
-cudaError_t launch_mx_gather(const uint8_t* xq, const uint8_t* xs, int T, int H, int k, const int32_t* pair_row,
-                             uint8_t* xpq, uint8_t* xps, cudaStream_t s);
+// the x rows of the tokens with local slots, quantised once per token, into the grouped rows
+cudaError_t launch_mx_dispatch_quantize(const uint16_t* x, int T, int H, int k, const int32_t* pair_row,
+                                       uint8_t* xpq, uint8_t* xps, cudaStream_t s);
 size_t mx_ffn_scratch_bytes(long long rows, int I);  // h codes + h scales
 cudaError_t launch_mx_expert_ffn(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets, const uint8_t* wgq,
                                  const uint8_t* wgs, const uint8_t* wuq, const uint8_t* wus, const uint8_t* wdq,

@@ -39,12 +39,14 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint4* __restric
     q[b * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-// ------------------------------------------------------------------ gather
-// one CTA per token: its E4M3 row (H16 16-byte vectors) and scale words (S4 per row)
+// ------------------------------------------------------------------ dispatch copy
+// one CTA per token: its x row is quantised to MXFP8 once (one 32-element block per
+// thread, the arithmetic of mx_quantize_kernel) and the codes and scale of each block
 // go to every grouped row of its local slots
-__global__ void __launch_bounds__(128) mx_gather_kernel(const uint4* __restrict__ xq, const uint32_t* __restrict__ xs,
-                                                        int H16, int S4, int k, const int32_t* __restrict__ pair_row,
-                                                        uint4* __restrict__ xpq, uint32_t* __restrict__ xps) {
+__global__ void __launch_bounds__(128) mx_dispatch_quantize_kernel(const uint4* __restrict__ x, int H, int k,
+                                                                   const int32_t* __restrict__ pair_row,
+                                                                   uint8_t* __restrict__ xpq,
+                                                                   uint8_t* __restrict__ xps) {
     __shared__ int rows[32];
     __shared__ int nrows;
     const int t = blockIdx.x;
@@ -57,13 +59,29 @@ __global__ void __launch_bounds__(128) mx_gather_kernel(const uint4* __restrict_
     __syncthreads();
     const int nr = nrows;
     if (nr == 0) return;
-    for (int v = threadIdx.x; v < H16; v += blockDim.x) {
-        const uint4 val = __ldg(xq + (size_t)t * H16 + v);
-        for (int i = 0; i < nr; ++i) xpq[(size_t)rows[i] * H16 + v] = val;
-    }
-    for (int v = threadIdx.x; v < S4; v += blockDim.x) {
-        const uint32_t sv = __ldg(xs + (size_t)t * S4 + v);
-        for (int i = 0; i < nr; ++i) xps[(size_t)rows[i] * S4 + v] = sv;
+    const int nblk = H / 32;
+    const uint4* src = x + (size_t)t * (H / 8);
+    for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 u = __ldg(src + b * 4 + i);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[8 * i + 2 * j] = bf16_lo(w4[j]);
+                v[8 * i + 2 * j + 1] = bf16_hi(w4[j]);
+            }
+        }
+        uint32_t w[8];
+        const uint8_t code = (uint8_t)mx::mx_quantize32(v, w);
+        for (int i = 0; i < nr; ++i) {
+            const size_t row = (size_t)rows[i];
+            uint4* dst = reinterpret_cast<uint4*>(xpq + row * H + 32 * b);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            xps[row * nblk + b] = code;
+        }
     }
 }
 
@@ -507,11 +525,9 @@ cudaError_t launch_mx_quantize(const uint16_t* src, long long rows, int K, uint8
     return cudaGetLastError();
 }
 
-cudaError_t launch_mx_gather(const uint8_t* xq, const uint8_t* xs, int T, int H, int k, const int32_t* pair_row,
-                             uint8_t* xpq, uint8_t* xps, cudaStream_t s) {
-    mx_gather_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(xq), reinterpret_cast<const uint32_t*>(xs),
-                                       H / 16, H / 128, k, pair_row, reinterpret_cast<uint4*>(xpq),
-                                       reinterpret_cast<uint32_t*>(xps));
+cudaError_t launch_mx_dispatch_quantize(const uint16_t* x, int T, int H, int k, const int32_t* pair_row,
+                                       uint8_t* xpq, uint8_t* xps, cudaStream_t s) {
+    mx_dispatch_quantize_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), H, k, pair_row, xpq, xps);
     return cudaGetLastError();
 }
 
