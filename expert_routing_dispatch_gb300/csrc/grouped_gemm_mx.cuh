@@ -422,7 +422,9 @@ __device__ __forceinline__ void run(Ctl<G::STAGES>& c, uint32_t ring, Pipe& pipe
                     row = b_row + 32 * i;
                     src = args.b0_s;
                 }
-                w[4 + i] = row < b_total ? __ldcg(src + row * args.kblocks + kb) : 0u;
+                // weight scales are read-only in every launch: cached loads, and the 32 (or 12)
+                // k-blocks of a tile read the same lines
+                w[4 + i] = row < b_total ? __ldg(src + row * args.kblocks + kb) : 0u;
             }
             return true;
         };
